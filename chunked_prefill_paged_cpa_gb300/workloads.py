@@ -1,0 +1,193 @@
+"""Named hybrid-batch workloads and the host state that feeds them.
+
+Every workload is composed by the decode-first scheduler (``sched``) from a
+set of requests and a token budget, so each step is what that policy would
+schedule.  Shapes are Llama-3-8B's attention (32 query heads, 8 KV heads,
+head_dim 128, bf16, 16-token pages) except the tiny parity case.
+
+* tiny            -- fp32, Hq 4 / Hkv 2 / D 64.  Request A: 96-token prompt
+                     prefilled 32 tokens per step; request B: 40 cached
+                     tokens, decoding.  Budget 33: steps 1-3 hold B's decode
+                     and one A chunk each, step 4 holds both decodes.
+* page1_default   -- 32 decodes (context ~U[512, 4096]) + one 480-token chunk
+                     of an 8192-token prompt at offset 3840 (budget 512): one
+                     layer of deepconcepts.dev's default simulated pass.
+* large_budget    -- 4 decodes (~U[1024, 8192]) + a 2048-token chunk at offset
+                     6144 (budget 2052).
+* oneshot_8192    -- the unchunked 8192-token prefill (budget 8192).
+* large_budget_chunked -- the same prompt as four 2048-token chunks from
+                     offset 0 beside the 4 decodes (chunked == one-shot check).
+* long_context    -- 64 decodes (~U[2048, 16384]) + a 512-token chunk of a
+                     32768-token prompt at offset 31744 (budget 576).
+* decode_only     -- 256 decodes (~U[2048, 8192]); the bandwidth case.
+
+Decode context lengths are the sequence's length after this step's token is
+appended.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+from . import synth
+from .batch import PageAllocator, PagedSeqs, build_metadata, write_positions, pages_for
+from .sched import Request, StepPlan, commit, schedule_step
+
+
+@dataclass
+class AttnShape:
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    dtype: torch.dtype
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+LLAMA3_8B = AttnShape(32, 8, 128, 16, torch.bfloat16)
+TINY = AttnShape(4, 2, 64, 16, torch.float32)
+
+
+@dataclass
+class Scenario:
+    name: str
+    shape: AttnShape
+    plans: list[StepPlan]
+    lifetimes: dict          # rid -> tokens the sequence will ever hold
+    q_from: dict             # rid -> first position whose query is needed
+    seed: int
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def rids(self) -> list[str]:
+        return list(self.lifetimes.keys())
+
+
+def _run(name, shape, running, waiting, budget, steps, seed, notes=None):
+    """Schedule ``steps`` passes and record what each sequence needs."""
+    plans, first_q, last_len = [], {}, {}
+    for _ in range(steps):
+        plan = schedule_step(running, waiting, budget)
+        for s in plan.seqs:
+            first_q.setdefault(s.rid, s.seq_len - s.q_len)
+            last_len[s.rid] = s.seq_len
+        plans.append(plan)
+        commit(plan, running, waiting)
+    return Scenario(name, shape, plans, last_len, first_q, seed, notes or {})
+
+
+def _decoders(lengths, prefix="d"):
+    # a decode whose context after this step is L has L - 1 tokens cached
+    return [Request(f"{prefix}{i}", L - 1, L - 1) for i, L in enumerate(lengths)]
+
+
+def scenario(name: str, seed: int = 0) -> Scenario:
+    s_len = seed * 1000 + 1
+    if name == "tiny":
+        running = [Request("B", 40, 40)]
+        waiting = [Request("A", 96, 0)]
+        return _run(name, TINY, running, waiting, 33, 4, seed,
+                    {"budget": 33})
+    if name == "page1_default":
+        L = synth.uniform_lengths(32, 512, 4096, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [Request("P", 8192, 3840)], 512,
+                    1, seed, {"budget": 512, "prompt": 8192, "offset": 3840})
+    if name == "large_budget":
+        L = synth.uniform_lengths(4, 1024, 8192, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [Request("P", 8192, 6144)], 2052,
+                    1, seed, {"budget": 2052, "prompt": 8192, "offset": 6144})
+    if name == "large_budget_chunked":
+        L = synth.uniform_lengths(4, 1024, 8192, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [Request("P", 8192, 0)], 2052,
+                    4, seed, {"budget": 2052, "prompt": 8192})
+    if name == "oneshot_8192":
+        return _run(name, LLAMA3_8B, [], [Request("P", 8192, 0)], 8192, 1, seed,
+                    {"budget": 8192, "prompt": 8192})
+    if name == "long_context":
+        L = synth.uniform_lengths(64, 2048, 16384, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [Request("P", 32768, 31744)], 576,
+                    1, seed, {"budget": 576, "prompt": 32768, "offset": 31744})
+    if name == "decode_only":
+        L = synth.uniform_lengths(256, 2048, 8192, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [], 256, 1, seed, {"budget": 256})
+    raise KeyError(name)
+
+
+NAMES = ["tiny", "page1_default", "large_budget", "long_context", "decode_only"]
+
+
+class WorkloadState:
+    """Device-resident state of a scenario: per-position Q/K/V, the page pool
+    (physical pages in random order, 1.25x the need, unused pages poisoned with
+    NaN), and the paged caches holding every sequence's prefix as the first
+    step finds it.  Steps are then fed in order; the caller appends each step's
+    new K/V (``cpa_kv_append``) before attending."""
+
+    def __init__(self, sc: Scenario, device="cpu", pool_factor: float = 1.25,
+                 tensor_device=None):
+        self.sc = sc
+        sh = sc.shape
+        self.device = torch.device(device)
+        rids = sc.rids
+        self.index = {r: i for i, r in enumerate(rids)}
+        tdev = tensor_device or device
+        self.seqs = synth.draw_sequences([sc.lifetimes[r] for r in rids],
+                                         [sc.q_from[r] for r in rids],
+                                         sh.num_q_heads, sh.num_kv_heads,
+                                         sh.head_dim, sh.dtype,
+                                         sc.seed * 1000 + 3, tdev)
+        need = sum(pages_for(sc.lifetimes[r], sh.page_size) for r in rids)
+        pool = max(1, math.ceil(need * pool_factor))
+        self.alloc = PageAllocator(synth.permutation(pool, sc.seed * 1000 + 2))
+        self.paged = PagedSeqs(self.alloc, sh.page_size)
+        self.num_pages = pool
+        cache_shape = (pool, sh.num_kv_heads, sh.page_size, sh.head_dim)
+        self.k_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
+                                  device=self.device)
+        self.v_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
+                                  device=self.device)
+        # prefix each sequence already has in the cache when it first appears
+        for plan in sc.plans:
+            for s in plan.seqs:
+                if s.rid in self.paged.pages:
+                    continue
+                pre = s.seq_len - s.q_len
+                pl = self.paged.ensure(s.rid, pre)
+                if pre > 0:
+                    pos = torch.arange(pre)
+                    k, v = self.kv_rows(s.rid, pos)
+                    write_positions(self.k_cache, self.v_cache, pl, pos, k, v)
+
+    def kv_rows(self, rid, positions: torch.Tensor):
+        i = self.index[rid]
+        rows = (self.seqs.kv_offsets[i] + positions).to(self.seqs.k.device)
+        return self.seqs.k[rows], self.seqs.v[rows]
+
+    def q_rows(self, rid, positions: torch.Tensor):
+        i = self.index[rid]
+        rows = (self.seqs.q_offsets[i] - self.seqs.q_from[i] + positions)
+        return self.seqs.q[rows.to(self.seqs.q.device)]
+
+    def step(self, k: int, max_pages: int | None = None) -> dict:
+        """Inputs of step k: metadata (on the state's device), packed q and the
+        new tokens' k/v ([T, H, D])."""
+        plan = self.sc.plans[k]
+        page_lists = [self.paged.ensure(s.rid, s.seq_len) for s in plan.seqs]
+        meta = build_metadata(plan.q_lens, plan.seq_lens, page_lists,
+                              self.sc.shape.page_size, self.num_pages, max_pages)
+        qs, ks, vs = [], [], []
+        for s in plan.seqs:
+            pos = torch.arange(s.seq_len - s.q_len, s.seq_len)
+            qs.append(self.q_rows(s.rid, pos))
+            kk, vv = self.kv_rows(s.rid, pos)
+            ks.append(kk)
+            vs.append(vv)
+        dev = self.device
+        return {"meta": meta.to(dev), "q": torch.cat(qs).to(dev).contiguous(),
+                "k": torch.cat(ks).to(dev).contiguous(),
+                "v": torch.cat(vs).to(dev).contiguous(), "plan": plan}

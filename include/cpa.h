@@ -1,0 +1,128 @@
+/*
+ * cpa.h -- C ABI of libcpa: one chunked-prefill attention step over a paged
+ * KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The step ("vllm-learning-book 05. Chunked Prefill", sections 3 and 4):
+ * a packed hybrid batch of S sequences whose scheduled tokens are concatenated
+ * on one token axis with no padding.  Sequence s owns packed tokens
+ * query_start_loc[s] .. query_start_loc[s+1]-1 (q_len of them) and holds
+ * seq_lens[s] tokens in the cache once this step's K/V are appended.  A
+ * prefill chunk has q_len > 1; a decode has q_len == 1.  Query row i of
+ * sequence s attends to cache positions 0 .. seq_lens[s]-q_len+i: every
+ * earlier chunk's K/V plus a causal mask inside the chunk (same page, Q&A of
+ * section 8; "Chunked Prefill 技术深度解析", section 4.1).
+ *
+ * Conventions shared by every call
+ *  - All pointers are device pointers unless a comment says otherwise.  The
+ *    caller owns and allocates every buffer; the library never allocates
+ *    device memory, never synchronises the stream, and keeps no state
+ *    between calls besides the workspace the caller passes in.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid argument returns a negative cpa_status and launches nothing.
+ *  - Layouts (row-major, contiguous):
+ *      q, out            [num_tokens][num_q_heads][head_dim]
+ *      k, v (new tokens) [num_tokens][num_kv_heads][head_dim]
+ *      k_cache, v_cache  [num_pages][num_kv_heads][page_size][head_dim]
+ *      block_table       int32 [num_seqs][max_pages_per_seq]
+ *      query_start_loc   int32 [num_seqs + 1], query_start_loc[0] == 0
+ *      seq_lens          int32 [num_seqs]
+ *      slot_mapping      int64 [num_tokens]
+ *    Element type of q, k, v, caches and out: `dtype` (fp32 or bf16).
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Supported: head_dim 64 or 128, page_size 16, num_q_heads a multiple of
+ *    num_kv_heads with a group of 1, 2, 4 or 8 heads.
+ */
+#ifndef CPA_H
+#define CPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CPA_OK = 0,
+  CPA_ERR_ARG = -1,          /* malformed argument (null pointer, bad size)    */
+  CPA_ERR_UNSUPPORTED = -2,  /* valid but not supported (e.g. head_dim 96)     */
+  CPA_ERR_WORKSPACE = -3,    /* workspace missing, misaligned or too small     */
+  CPA_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed           */
+  CPA_ERR_DEVICE = -5        /* a kernel found an out-of-range index (status
+                                word, read back with cpa_read_device_status)  */
+} cpa_status;
+
+typedef enum { CPA_F32 = 0, CPA_BF16 = 1 } cpa_dtype;
+
+/* Problem description shared by the calls.  Sizes are host values. */
+typedef struct cpa_desc {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int64_t num_pages;          /* pages in each of k_cache / v_cache           */
+  int32_t max_pages_per_seq;  /* row stride of block_table; also bounds
+                                 seq_lens[s] <= max_pages_per_seq * page_size */
+  int32_t dtype;              /* cpa_dtype                                    */
+  int64_t num_tokens;         /* packed tokens this step (query_start_loc[S]) */
+  void *workspace;            /* device scratch, >= cpa_workspace_bytes(),
+                                 256-byte aligned, zero-filled before its first
+                                 use; every completed attention call leaves it
+                                 ready for the next one                       */
+  size_t workspace_bytes;
+} cpa_desc;
+
+/* Human-readable name of a cpa_status value (static string, never NULL). */
+const char *cpa_status_string(int status);
+
+/* Bytes of workspace cpa_attention_forward needs for at most `num_seqs`
+ * sequences with this description.  Pure host arithmetic; returns 0 if the
+ * description is invalid.  The workspace holds the split-KV partial results
+ * (o, running max, running sum) of long decodes, the per-(sequence, kv head)
+ * arrival counters of the in-launch merge, and a device status word. */
+size_t cpa_workspace_bytes(const cpa_desc *desc, int32_t num_seqs);
+
+/* KV append: for every packed token t with slot = slot_mapping[t] >= 0, copy
+ * k[t][g][:] to k_cache[slot / page_size][g][slot % page_size][:] and likewise
+ * v, for all kv heads g.  A negative slot skips the token.  The copy is
+ * bit-exact.  ("Chunked Prefill on an M5 Max", section "Wiring it into the
+ * loop": a chunk extends the cache instead of rebuilding it; "Chunked Prefill
+ * 技术深度解析", section 4.2: 16-token pages.)
+ * Slots >= num_pages * page_size are skipped and raise the device status word
+ * when a workspace is given in desc.  Tokens must map to distinct slots.
+ * Only desc->num_kv_heads, head_dim, page_size, num_pages, dtype, num_tokens
+ * and (optionally) workspace are read. */
+int cpa_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
+                  void *k_cache, void *v_cache, const cpa_desc *desc,
+                  void *stream);
+
+/* Attention forward of the whole hybrid batch in one call: out[t][h][:] =
+ * softmax(scale * q[t][h] . K_j) . V_j over the visible cache positions j of
+ * t's sequence (see the top of this file).  K/V are read through
+ * block_table; the step's own new K/V must already be in the cache
+ * (cpa_kv_append first).  Requires 1 <= q_len <= seq_lens[s] for every
+ * sequence and seq_lens[s] <= max_pages_per_seq * page_size; entries of
+ * block_table outside [0, num_pages) are not read and raise the device status
+ * word.  Decodes with long contexts are split over the KV axis and merged in
+ * the same launch with log-sum-exp weights ("Chunked Prefill 技术深度解析",
+ * section 7.2: softmax normalised over the visible keys and combined
+ * incrementally).  fp32 accumulation throughout; out has q's dtype. */
+int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_table,
+                          const int32_t *query_start_loc, const int32_t *seq_lens,
+                          int32_t num_seqs, float scale, void *out, void *stream,
+                          const cpa_desc *desc);
+
+/* Synchronously read (and clear) the device status word held in the
+ * workspace: CPA_OK, or CPA_ERR_DEVICE if a kernel since the last read met an
+ * out-of-range page or slot index.  Waits for `stream`.  Test/debug helper,
+ * not meant for the hot path. */
+int cpa_read_device_status(const cpa_desc *desc, void *stream, int32_t *status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPA_H */
