@@ -1,0 +1,149 @@
+// C ABI of libcpa: argument validation, workspace layout and launches.
+// Declared and documented in include/cpa.h.
+#include <stdio.h>
+
+#include "cpa_internal.cuh"
+
+namespace cpa {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
+  WorkspaceLayout w{};
+  const int64_t max_keys = (int64_t)d.max_pages_per_seq * d.page_size;
+  w.max_splits = (int)((max_keys + kSplitKeys - 1) / kSplitKeys);
+  if (w.max_splits < 1) w.max_splits = 1;
+  size_t off = 256;  // header
+  w.counters = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)num_seqs * d.num_kv_heads, 256);
+  w.part_o = off;
+  const size_t slots = (size_t)num_seqs * d.num_q_heads * w.max_splits;
+  off = align_up(off + sizeof(float) * slots * d.head_dim, 256);
+  w.part_ml = off;
+  off = align_up(off + sizeof(float2) * slots, 256);
+  w.total = off;
+  return w;
+}
+
+// Shape checks shared by both calls.
+static int check_shape(const cpa_desc *d) {
+  if (!d) return CPA_ERR_ARG;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
+      d->page_size <= 0 || d->num_pages <= 0 || d->num_tokens < 0)
+    return CPA_ERR_ARG;
+  if (d->num_q_heads % d->num_kv_heads != 0) return CPA_ERR_ARG;
+  if (d->dtype != CPA_F32 && d->dtype != CPA_BF16) return CPA_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return CPA_ERR_UNSUPPORTED;
+  if (d->page_size != 16) return CPA_ERR_UNSUPPORTED;
+  const int G = d->num_q_heads / d->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return CPA_ERR_UNSUPPORTED;
+  if (d->num_tokens > INT32_MAX / 2) return CPA_ERR_UNSUPPORTED;
+  return CPA_OK;
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace cpa
+
+using namespace cpa;
+
+extern "C" const char *cpa_status_string(int status) {
+  switch (status) {
+    case CPA_OK: return "CPA_OK";
+    case CPA_ERR_ARG: return "CPA_ERR_ARG: malformed argument";
+    case CPA_ERR_UNSUPPORTED: return "CPA_ERR_UNSUPPORTED: shape or dtype not supported";
+    case CPA_ERR_WORKSPACE: return "CPA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case CPA_ERR_CUDA: return "CPA_ERR_CUDA: CUDA runtime or launch error";
+    case CPA_ERR_DEVICE: return "CPA_ERR_DEVICE: a kernel met an out-of-range index";
+    default: return "unknown cpa_status";
+  }
+}
+
+extern "C" size_t cpa_workspace_bytes(const cpa_desc *desc, int32_t num_seqs) {
+  if (check_shape(desc) != CPA_OK || num_seqs < 0 || desc->max_pages_per_seq <= 0) return 0;
+  return workspace_layout(*desc, num_seqs).total;
+}
+
+extern "C" int cpa_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
+                             void *k_cache, void *v_cache, const cpa_desc *desc,
+                             void *stream) {
+  int rc = check_shape(desc);
+  if (rc != CPA_OK) return rc;
+  if (desc->num_tokens == 0) return CPA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return CPA_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return CPA_ERR_ARG;
+  uint32_t *status = nullptr;
+  if (desc->workspace) {
+    if (!aligned(desc->workspace, 256) || desc->workspace_bytes < 256) return CPA_ERR_WORKSPACE;
+    status = static_cast<uint32_t *>(desc->workspace);
+  }
+  const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
+  cudaError_t e = launch_kv_append(k, v, slot_mapping, k_cache, v_cache, desc->num_tokens,
+                                   desc->num_kv_heads, desc->head_dim, desc->page_size,
+                                   desc->num_pages, eb, status, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+}
+
+extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_table,
+                                     const int32_t *query_start_loc, const int32_t *seq_lens,
+                                     int32_t num_seqs, float scale, void *out, void *stream,
+                                     const cpa_desc *desc) {
+  int rc = check_shape(desc);
+  if (rc != CPA_OK) return rc;
+  if (num_seqs < 0) return CPA_ERR_ARG;
+  if (num_seqs == 0 || desc->num_tokens == 0) return CPA_OK;
+  if (desc->num_tokens < num_seqs) return CPA_ERR_ARG;  // every sequence has q_len >= 1
+  if (!q || !k_cache || !v_cache || !block_table || !query_start_loc || !seq_lens || !out)
+    return CPA_ERR_ARG;
+  if (desc->max_pages_per_seq <= 0) return CPA_ERR_ARG;
+  if (!(scale > 0.f) || scale != scale) return CPA_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(block_table, 4) || !aligned(query_start_loc, 4) || !aligned(seq_lens, 4))
+    return CPA_ERR_ARG;
+  const WorkspaceLayout w = workspace_layout(*desc, num_seqs);
+  if (!desc->workspace || !aligned(desc->workspace, 256) || desc->workspace_bytes < w.total)
+    return CPA_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(desc->workspace);
+
+  AttnParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_table = block_table;
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.num_seqs = num_seqs;
+  p.num_tokens = (int)desc->num_tokens;
+  p.Hq = desc->num_q_heads;
+  p.Hkv = desc->num_kv_heads;
+  p.D = desc->head_dim;
+  p.page_size = desc->page_size;
+  p.num_pages = desc->num_pages;
+  p.max_pages = desc->max_pages_per_seq;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.max_splits = w.max_splits;
+  p.status = reinterpret_cast<uint32_t *>(ws);
+  p.counters = reinterpret_cast<uint32_t *>(ws + w.counters);
+  p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+  p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
+  cudaError_t e = launch_attention_rows(p, desc->dtype, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+}
+
+extern "C" int cpa_read_device_status(const cpa_desc *desc, void *stream, int32_t *status_out) {
+  if (!desc || !desc->workspace || !status_out) return CPA_ERR_ARG;
+  if (!aligned(desc->workspace, 256) || desc->workspace_bytes < 256) return CPA_ERR_WORKSPACE;
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, desc->workspace, sizeof word, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return CPA_ERR_CUDA;
+  if (cudaMemsetAsync(desc->workspace, 0, sizeof word, s) != cudaSuccess) return CPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CPA_ERR_CUDA;
+  *status_out = word ? CPA_ERR_DEVICE : CPA_OK;
+  return CPA_OK;
+}

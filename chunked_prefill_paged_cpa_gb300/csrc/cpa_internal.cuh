@@ -1,0 +1,66 @@
+// Internal declarations shared by the libcpa translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "cpa.h"
+
+namespace cpa {
+
+// Device status bits (OR-ed into the status word at the start of the
+// workspace; host reads it with cpa_read_device_status).
+enum : uint32_t {
+  STATUS_BAD_PAGE = 1u,   // block_table entry outside [0, num_pages)
+  STATUS_BAD_SLOT = 2u,   // slot_mapping entry >= num_pages * page_size
+  STATUS_TIMEOUT = 4u,    // a bounded wait gave up
+};
+
+// Workspace layout (byte offsets from desc->workspace, all 256-aligned):
+//   [0, 256)            header: uint32 status word, uint32 work counters
+//   counters            uint32 [num_seqs * Hkv]   split-merge arrival counts
+//   part_o              float  [num_seqs * Hq * max_splits * D]
+//   part_ml             float2 [num_seqs * Hq * max_splits]  (max, sum)
+struct WorkspaceLayout {
+  size_t counters, part_o, part_ml, total;
+  int max_splits;
+};
+
+// Keys handled by one split of a long decode.
+constexpr int kSplitKeys = 512;
+
+WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs);
+
+struct AttnParams {
+  const void *q;
+  const void *k_cache;
+  const void *v_cache;
+  const int32_t *block_table;
+  const int32_t *query_start_loc;
+  const int32_t *seq_lens;
+  void *out;
+  int num_seqs;
+  int num_tokens;
+  int Hq, Hkv, D, page_size;
+  int64_t num_pages;
+  int max_pages;
+  float scale_log2;          // scale * log2(e): scores live in the log2 domain
+  int max_splits;
+  uint32_t *status;
+  uint32_t *counters;
+  float *part_o;
+  float2 *part_ml;
+};
+
+cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
+                             void *k_cache, void *v_cache, int64_t num_tokens,
+                             int Hkv, int D, int page_size, int64_t num_pages,
+                             int elem_bytes, uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t stream);
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+}  // namespace cpa

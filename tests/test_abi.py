@@ -1,0 +1,100 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed:
+none of these calls reaches the device)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from chunked_prefill_paged_cpa_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(cpa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ops.load(build_if_missing=True)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("cpa_kv_append", "cpa_attention_forward", "cpa_workspace_bytes",
+                     "cpa_status_string", "cpa_read_device_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _desc(**kw):
+    d = ops.CpaDesc(32, 8, 128, 16, 1000, 64, ops.CPA_BF16, 10, None, 0)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert ops.cpa_status_string(code).startswith("CPA_")
+    assert "unknown" in ops.cpa_status_string(7)
+
+
+def test_workspace_bytes_host_arithmetic(lib):
+    d = _desc()
+    n1 = ops.cpa_workspace_bytes(d, 1)
+    n256 = ops.cpa_workspace_bytes(d, 256)
+    assert n1 >= 256 and n256 > n1 and n256 % 256 == 0
+    assert ops.cpa_workspace_bytes(_desc(head_dim=96), 4) == 0
+    assert ops.cpa_workspace_bytes(_desc(num_q_heads=30), 4) == 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, ops.CPA_ERR_UNSUPPORTED),
+    ("page_size", 32, ops.CPA_ERR_UNSUPPORTED),
+    ("num_q_heads", 12, ops.CPA_ERR_ARG),       # not a multiple of 8 kv heads
+    ("num_q_heads", 8 * 16, ops.CPA_ERR_UNSUPPORTED),  # group of 16
+    ("dtype", 5, ops.CPA_ERR_UNSUPPORTED),
+    ("num_pages", 0, ops.CPA_ERR_ARG),
+])
+def test_bad_descriptor_rejected_before_launch(lib, field, value, code):
+    d = _desc(**{field: value})
+    P = ctypes.c_void_p(256)
+    assert ops.cpa_kv_append(P, P, P, P, P, d, None) == code
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 2, 0.1, P, None, d) == code
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    d = _desc()
+    P = ctypes.c_void_p(4096)
+    assert ops.cpa_kv_append(None, P, P, P, P, d, None) == ops.CPA_ERR_ARG
+    assert ops.cpa_kv_append(ctypes.c_void_p(4100), P, P, P, P, d, None) == ops.CPA_ERR_ARG
+    assert ops.cpa_attention_forward(P, P, P, None, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    # missing workspace
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_WORKSPACE
+    # too small workspace
+    d.workspace, d.workspace_bytes = 4096, 512
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_WORKSPACE
+    # bad scale and more sequences than tokens
+    d.workspace_bytes = 1 << 30
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 2, -1.0, P, None, d) == ops.CPA_ERR_ARG
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 11, 0.1, P, None, d) == ops.CPA_ERR_ARG
+
+
+def test_empty_step_is_a_no_op(lib):
+    d = _desc(num_tokens=0)
+    P = ctypes.c_void_p(4096)
+    assert ops.cpa_kv_append(P, P, P, P, P, d, None) == ops.CPA_OK
+    assert ops.cpa_attention_forward(P, P, P, P, P, P, 0, 0.1, P, None, d) == ops.CPA_OK

@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars (bf16 in, fp32 accumulate): attention within max-abs 2e-2 and mean-abs
+2e-3 of the oracle; KV append and page addressing bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_prefill_paged_cpa_gb300 import ops, workloads
+from chunked_prefill_paged_cpa_gb300.batch import pages_for
+from support import make_step, oracle_state_for, to_np64
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+
+
+def assert_close(got, want, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    assert err.max() <= MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+
+
+def bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def gpu_step(k_cache, v_cache, inp, scale, Hq, workspace=None):
+    m = inp["meta"]
+    ops.kv_append(inp["k"], inp["v"], m.slot_mapping, k_cache, v_cache)
+    if workspace is None:
+        workspace = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs)
+    out = ops.attention_forward(inp["q"], k_cache, v_cache, m.block_table,
+                                m.query_start_loc, m.seq_lens, scale, workspace)
+    return out, workspace
+
+
+def test_tiny_all_steps_match_oracle_and_cache_is_bitexact(cuda_device):
+    sc = workloads.scenario("tiny")
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    oc = oracle_state_for(ws)
+    sh = sc.shape
+    # the prefix fill must already agree bit for bit
+    assert torch.equal(bits(ws.k_cache.cpu()), bits(oc.k))
+    for k in range(len(sc.plans)):
+        inp = ws.step(k)
+        m = inp["meta"]
+        out, wsp = gpu_step(ws.k_cache, ws.v_cache, inp, sh.scale, sh.num_q_heads)
+        oc.append(m.block_table.cpu(), m.q_lens, m.seq_lens_list, inp["k"].cpu(),
+                  inp["v"].cpu())
+        assert torch.equal(bits(ws.k_cache.cpu()), bits(oc.k)), f"step {k}: K cache"
+        assert torch.equal(bits(ws.v_cache.cpu()), bits(oc.v)), f"step {k}: V cache"
+        want = oracle.attention(inp["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                                m.seq_lens, sh.scale)
+        assert_close(out.cpu(), want, f"tiny step {k + 1}")
+        assert ops.device_status(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], wsp) == 0
+
+
+def test_tiny_chunked_equals_oneshot_on_gpu(cuda_device):
+    """A's three 32-token chunks (steps 1-3) equal A's one-shot 96-token
+    prefill, and A's step-4 decode equals row 96 of a one-shot 97-token
+    prefill."""
+    sc = workloads.scenario("tiny")
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    sh = sc.shape
+    rows = []
+    for k in range(4):
+        inp = ws.step(k)
+        out, _ = gpu_step(ws.k_cache, ws.v_cache, inp, sh.scale, sh.num_q_heads)
+        qsl = inp["meta"].query_start_loc.cpu().tolist()
+        rids = [s.rid for s in inp["plan"].seqs]
+        a = rids.index("A")
+        rows.append(out[qsl[a]:qsl[a + 1]].cpu())
+    chunked = torch.cat(rows)                                   # positions 0..96
+    ws2 = workloads.WorkloadState(sc, device=cuda_device)
+    pl = ws2.paged.ensure("A", 97)
+    from chunked_prefill_paged_cpa_gb300.batch import build_metadata, write_positions
+    pos = torch.arange(97)
+    kk, vv = ws2.kv_rows("A", pos)
+    write_positions(ws2.k_cache, ws2.v_cache, pl, pos, kk, vv)
+    meta = build_metadata([97], [97], [pl], 16, ws2.num_pages).to(cuda_device)
+    wsp = ops.workspace_for(ws2.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1)
+    one = ops.attention_forward(ws2.q_rows("A", pos).to(cuda_device).contiguous(),
+                                ws2.k_cache, ws2.v_cache, meta.block_table,
+                                meta.query_start_loc, meta.seq_lens, sh.scale, wsp)
+    assert_close(chunked, one.cpu().double(), "chunked vs one-shot (GPU both)")
+
+
+SMALL_CASES = [
+    # (q_lens, seq_lens, Hq, Hkv, D, dtype)
+    ([1, 1, 1], [1, 17, 600], 8, 8, 128, torch.bfloat16),
+    ([33, 1, 129, 1], [50, 1100, 129, 3], 32, 8, 128, torch.bfloat16),
+    ([200], [1300], 16, 2, 128, torch.bfloat16),
+    ([5, 1, 64], [5, 2049, 100], 4, 2, 64, torch.float32),
+    ([1, 70, 1], [513, 70, 1025], 16, 2, 64, torch.bfloat16),
+    ([300, 1], [310, 4000], 8, 1, 128, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL_CASES)))
+def test_small_hybrid_batches(cuda_device, case):
+    q_lens, seq_lens, Hq, Hkv, D, dtype = SMALL_CASES[case]
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, dtype, seed=100 + case)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)   # prefix state (input), pre-append
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(D)
+    out, _ = gpu_step(k_cache, v_cache, inp, scale, Hq)
+    slots = oracle.slot_mapping(m.block_table, m.query_start_loc, m.seq_lens, 16)
+    assert torch.equal(slots, m.slot_mapping)
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], slots)
+    assert torch.equal(bits(k_cache.cpu()), bits(oc.k))
+    assert torch.equal(bits(v_cache.cpu()), bits(oc.v))
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    assert_close(out.cpu(), want, f"case {case}")
+
+
+def test_ones_values_give_ones_and_onehot_values_give_probabilities(cuda_device):
+    """V == 1 makes every output 1 (softmax rows sum to 1, including across
+    merged splits); V_j = e_j (ctx <= D) makes the output row the probability
+    row, compared with the oracle's probabilities."""
+    dev = cuda_device
+    q_lens, seq_lens, Hq, Hkv, D = [1, 20, 1], [1500, 60, 64], 8, 2, 64
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=7)
+    m, oc = st["meta"], st["oracle_cache"]
+    slots = m.slot_mapping
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], slots)
+    ones = torch.ones_like(oc.v).to(dev)
+    k_cache = oc.k.to(dev)
+    wsp = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs)
+    md = m.to(dev)
+    out = ops.attention_forward(st["q"].to(dev), k_cache, ones, md.block_table,
+                                md.query_start_loc, md.seq_lens, 0.125, wsp)
+    assert (out.float() - 1).abs().max().item() <= 2 ** -7
+    # one-hot values over the 64-token sequence (third sequence: a decode)
+    vh = torch.zeros_like(oc.v)
+    pl = m.block_table[2].tolist()
+    for j in range(64):
+        vh[pl[j // 16], :, j % 16, j] = 1.0
+    out = ops.attention_forward(st["q"].to(dev), k_cache, vh.to(dev), md.block_table,
+                                md.query_start_loc, md.seq_lens, 0.125, wsp)
+    t = int(m.query_start_loc[2])
+    for h in range(Hq):
+        p, _ = oracle.probs(st["q"], oc.k, vh, m.block_table, m.query_start_loc,
+                            m.seq_lens, 0.125, t, h)
+        got = out[t, h, :64].float().cpu().numpy()
+        assert np.abs(got - p).max() <= 4e-3, h
+
+
+def test_workspace_reuse_gives_identical_results(cuda_device):
+    sc = workloads.scenario("page1_default")
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    inp = ws.step(0)
+    out1, wsp = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, 32)
+    m = inp["meta"]
+    out2 = ops.attention_forward(inp["q"], ws.k_cache, ws.v_cache, m.block_table,
+                                 m.query_start_loc, m.seq_lens, sc.shape.scale, wsp)
+    assert torch.equal(bits(out1), bits(out2))
+
+
+def test_out_of_range_page_sets_status_without_fault(cuda_device):
+    dev = cuda_device
+    st = make_step([1, 4], [40, 20], 4, 2, 64, torch.float32, seed=3)
+    m, oc = st["meta"], st["oracle_cache"]
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    md = m.to(dev)
+    bt = md.block_table.clone()
+    bt[0, 1] = 10 ** 6                     # not a page of the pool
+    wsp = ops.workspace_for(k_cache, 4, bt.shape[1], 2)
+    ops.attention_forward(st["q"].to(dev), k_cache, v_cache, bt, md.query_start_loc,
+                          md.seq_lens, 0.125, wsp)
+    assert ops.device_status(k_cache, 4, bt.shape[1], wsp) == ops.CPA_ERR_DEVICE
+    assert ops.device_status(k_cache, 4, bt.shape[1], wsp) == ops.CPA_OK   # cleared
+    slots = md.slot_mapping.clone()
+    slots[0] = k_cache.shape[0] * 16 + 5   # past the pool
+    ops.kv_append(st["k_new"].to(dev), st["v_new"].to(dev), slots, k_cache, v_cache, wsp)
+    assert ops.device_status(k_cache, 4, bt.shape[1], wsp) == ops.CPA_ERR_DEVICE
+
+
+# ---- full-size workloads: sampled rows, per-sequence oracle ----------------
+
+def oracle_rows_for_seq(ws, rid, seq_len, q_len, rows):
+    """fp64 oracle output of rows ``rows`` (indices within the sequence's
+    q_len new tokens) computed from the generator's per-position tensors in a
+    fresh identity-paged host cache built by the oracle itself."""
+    sh = ws.sc.shape
+    n = pages_for(seq_len, sh.page_size)
+    kc = torch.full((n, sh.num_kv_heads, sh.page_size, sh.head_dim), float("nan"),
+                    dtype=sh.dtype)
+    vc = kc.clone()
+    bt = torch.arange(n, dtype=torch.int32).view(1, n)
+    allq = torch.tensor([0, seq_len], dtype=torch.int32)
+    sl = torch.tensor([seq_len], dtype=torch.int32)
+    pos = torch.arange(seq_len)
+    kk, vv = ws.kv_rows(rid, pos)
+    oracle.kv_append(kc, vc, kk.cpu(), vv.cpu(), oracle.slot_mapping(bt, allq, sl, sh.page_size))
+    q = ws.q_rows(rid, torch.arange(seq_len - q_len, seq_len)).cpu()
+    qsl = torch.tensor([0, q_len], dtype=torch.int32)
+    return oracle.attention(q, kc, vc, bt, qsl, sl, sh.scale, rows=rows)
+
+
+def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24):
+    sc = workloads.scenario(name)
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    inp = ws.step(0)
+    m = inp["meta"]
+    out, _ = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, sc.shape.num_q_heads)
+    torch.cuda.synchronize()
+    # paging bit-exact: the package's slots equal the oracle's, and the cache
+    # holds the new rows at exactly those slots
+    mc = m.to("cpu")
+    slots = oracle.slot_mapping(mc.block_table, mc.query_start_loc, mc.seq_lens, 16)
+    assert torch.equal(slots, mc.slot_mapping)
+    sd = slots.to(cuda_device)
+    got_k = ws.k_cache[sd // 16, :, sd % 16, :]
+    got_v = ws.v_cache[sd // 16, :, sd % 16, :]
+    assert torch.equal(bits(got_k), bits(inp["k"])) and torch.equal(bits(got_v), bits(inp["v"]))
+    # pages never handed out are still poisoned
+    used = torch.zeros(ws.num_pages, dtype=torch.bool)
+    for pl in ws.paged.pages.values():
+        used[pl] = True
+    unused = (~used).nonzero().flatten().to(cuda_device)
+    if unused.numel():
+        assert torch.isnan(ws.k_cache[unused].float()).all()
+    # sampled rows against the oracle
+    g = torch.Generator().manual_seed(11)
+    qsl = mc.query_start_loc.tolist()
+    seqs = inp["plan"].seqs
+    dec = [i for i, s in enumerate(seqs) if s.kind == "decode"]
+    pick = [dec[int(j)] for j in torch.randperm(len(dec), generator=g)[:n_decode_samples]]
+    pre = [i for i, s in enumerate(seqs) if s.kind == "prefill"]
+    got_all, want_all = [], []
+    for i in pick + pre:
+        s = seqs[i]
+        if s.q_len == 1:
+            rows = [0]
+        else:
+            rows = sorted(set([0, 1, s.q_len - 1] +
+                              torch.randint(0, s.q_len, (n_chunk_rows,), generator=g).tolist()))
+        want = oracle_rows_for_seq(ws, s.rid, s.seq_len, s.q_len, rows)
+        got = out[[qsl[i] + r for r in rows]].float().cpu().numpy()
+        assert_close(got, want, f"{name} seq {s.rid}")
+        got_all.append(got)
+        want_all.append(want)
+    assert_close(np.concatenate([g_.ravel() for g_ in got_all]),
+                 np.concatenate([w.ravel() for w in want_all]), name)
+
+
+@pytest.mark.parametrize("name", ["page1_default", "large_budget", "long_context",
+                                  "decode_only"])
+def test_full_size_config(name, cuda_device):
+    check_full_config(name, cuda_device)
