@@ -20,6 +20,10 @@ MAX_ABS, MEAN_ABS = 2e-2, 2e-3
 
 
 def assert_close(got, want, what=""):
+    if isinstance(got, torch.Tensor):
+        got = got.detach().to("cpu", torch.float64).numpy()
+    if isinstance(want, torch.Tensor):
+        want = want.detach().to("cpu", torch.float64).numpy()
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert np.isfinite(got).all(), f"{what}: non-finite output"
