@@ -73,6 +73,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.cpa_kv_append.restype = ctypes.c_int
         lib.cpa_attention_forward.argtypes = [P, P, P, P, P, P, I32, F, P, P, D]
         lib.cpa_attention_forward.restype = ctypes.c_int
+        lib.cpa_attention_forward_noalloc.argtypes = [P, P, P, P, P, P, I32, F, P, P, D]
+        lib.cpa_attention_forward_noalloc.restype = ctypes.c_int
         lib.cpa_read_device_status.argtypes = [D, P, ctypes.POINTER(I32)]
         lib.cpa_read_device_status.restype = ctypes.c_int
         _lib = lib
@@ -99,6 +101,21 @@ def cpa_attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq
     return int(load().cpa_attention_forward(q, k_cache, v_cache, block_table,
                                             query_start_loc, seq_lens, int(num_seqs),
                                             float(scale), out, stream, ctypes.byref(desc)))
+
+
+def cpa_attention_forward_noalloc(q, k_cache, v_cache, block_table, query_start_loc,
+                                  seq_lens, num_seqs, scale, out, stream,
+                                  desc: CpaDesc) -> int:
+    """Mirror of the C entry point for callers that cannot allocate device
+    memory: the scratch is a fixed array inside the library and
+    desc.workspace is ignored."""
+    return int(load().cpa_attention_forward_noalloc(q, k_cache, v_cache, block_table,
+                                                    query_start_loc, seq_lens, int(num_seqs),
+                                                    float(scale), out, stream,
+                                                    ctypes.byref(desc)))
+
+
+CPA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def cpa_read_device_status(desc: CpaDesc, stream) -> int:

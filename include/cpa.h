@@ -115,6 +115,42 @@ int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cach
                           int32_t num_seqs, float scale, void *out, void *stream,
                           const cpa_desc *desc);
 
+/* Size of the scratch array built into the library for
+ * cpa_attention_forward_noalloc: 16 MiB of device memory on every GPU that
+ * loads the library, held until the process exits. */
+#define CPA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Attention forward for callers that may not allocate device memory.  The
+ * pages have no counterpart to this call: it is a library convenience.
+ * Callers in this position include plugins inside a host runtime that owns
+ * all device memory and passes in only inputs and outputs, and serving loops
+ * that forbid cudaMalloc/cudaFree after start-up because those calls can
+ * synchronise the device and can fail under memory pressure mid-step.
+ *
+ * Same computation, arguments and layouts as cpa_attention_forward, except
+ * that desc->workspace and desc->workspace_bytes are ignored: the scratch
+ * lives in a fixed array compiled into the library.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *  - Limit: the workspace this step would need, cpa_workspace_bytes(desc,
+ *    num_seqs), must not exceed CPA_NOALLOC_SCRATCH_BYTES; larger steps are
+ *    rejected with CPA_ERR_WORKSPACE before anything is launched.
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address with cudaGetSymbolAddress and caches it;
+ *    make that first call before any stream capture.  CPA_ERR_CUDA if the
+ *    lookup fails.
+ *  - Sharing: every call on a device uses the same array, which keeps what the
+ *    last call left in it.  Each call clears the merge counters and the
+ *    status word on `stream` before its launch.  Calls whose work overlaps on
+ *    the GPU (different streams, or different host threads) race on the
+ *    array: serialise them.
+ *  - The device status word of these calls is internal; use
+ *    cpa_attention_forward with a workspace to read it. */
+int cpa_attention_forward_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_table,
+                                  const int32_t *query_start_loc, const int32_t *seq_lens,
+                                  int32_t num_seqs, float scale, void *out, void *stream,
+                                  const cpa_desc *desc);
+
 /* Synchronously read (and clear) the device status word held in the
  * workspace: CPA_OK, or CPA_ERR_DEVICE if a kernel since the last read met an
  * out-of-range page or slot index.  Waits for `stream`.  Test/debug helper,
