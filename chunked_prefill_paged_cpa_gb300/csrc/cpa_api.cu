@@ -10,6 +10,8 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
   WorkspaceLayout w{};
+  const int G = d.num_q_heads / d.num_kv_heads;
+  w.fast_decode = decode_fast_path(d.dtype, d.head_dim, G);
   const int64_t max_keys = (int64_t)d.max_pages_per_seq * d.page_size;
   w.max_splits = (int)((max_keys + kSplitKeys - 1) / kSplitKeys);
   if (w.max_splits < 1) w.max_splits = 1;
@@ -17,12 +19,31 @@ WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
   w.counters = off;
   off = align_up(off + sizeof(uint32_t) * (size_t)num_seqs * d.num_kv_heads, 256);
   w.part_o = off;
-  const size_t slots = (size_t)num_seqs * d.num_q_heads * w.max_splits;
-  off = align_up(off + sizeof(float) * slots * d.head_dim, 256);
+  size_t rows;  // partial rows of head_dim floats
+  if (w.fast_decode) {
+    rows = ((size_t)num_seqs * d.num_kv_heads + kDecodeMaxWorkers) * G;
+  } else {
+    rows = (size_t)num_seqs * d.num_q_heads * w.max_splits;
+  }
+  off = align_up(off + sizeof(float) * rows * d.head_dim, 256);
   w.part_ml = off;
-  off = align_up(off + sizeof(float2) * slots, 256);
+  off = align_up(off + sizeof(float2) * rows, 256);
   w.total = off;
   return w;
+}
+
+int decode_grid(int device) {
+  static int sms[64] = {};
+  if (device < 0 || device >= 64) return 0;
+  if (!sms[device]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    sms[device] = n;
+  }
+  return sms[device];
 }
 
 // Shape checks shared by both calls.
@@ -130,7 +151,21 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
   p.counters = reinterpret_cast<uint32_t *>(ws + w.counters);
   p.part_o = reinterpret_cast<float *>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
-  cudaError_t e = launch_attention_rows(p, desc->dtype, (cudaStream_t)stream);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (w.fast_decode) {
+    if (num_seqs > kDecodeMaxSeqs) return CPA_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
+    int grid = decode_grid(dev);
+    if (grid <= 0) return CPA_ERR_CUDA;
+    if (grid * 8 > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / 8;
+    cudaError_t e = launch_attention_decode(p, grid, st);
+    if (e != cudaSuccess) return CPA_ERR_CUDA;
+    if (p.num_tokens == num_seqs) return CPA_OK;  // every sequence is a decode
+    p.skip_decode = 1;
+  }
+  cudaError_t e = launch_attention_rows(p, desc->dtype, st);
   return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }
 

@@ -18,17 +18,24 @@ enum : uint32_t {
 };
 
 // Workspace layout (byte offsets from desc->workspace, all 256-aligned):
-//   [0, 256)            header: uint32 status word, uint32 work counters
-//   counters            uint32 [num_seqs * Hkv]   split-merge arrival counts
-//   part_o              float  [num_seqs * Hq * max_splits * D]
-//   part_ml             float2 [num_seqs * Hq * max_splits]  (max, sum)
+//   [0, 256)   header: uint32 status word
+//   counters   uint32 [num_seqs * Hkv]   split-merge arrival counts
+//   part_o     split partial outputs (float), part_ml their (max, sum) pairs.
+// With the streaming decode kernel (bf16 fast path) a partial slot holds the
+// G rows of one (sequence, kv head) contribution and there are
+// num_seqs * Hkv + kDecodeMaxWorkers slots; otherwise the row kernel keeps
+// one slot per (sequence, query head, split).
 struct WorkspaceLayout {
   size_t counters, part_o, part_ml, total;
   int max_splits;
+  bool fast_decode;
 };
 
-// Keys handled by one split of a long decode.
+// Keys handled by one split of a long decode in the row kernel.
 constexpr int kSplitKeys = 512;
+// Streaming decode kernel limits.
+constexpr int kDecodeMaxSeqs = 4096;
+constexpr int kDecodeMaxWorkers = 4096;  // CTAs x warps of its persistent grid
 
 WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs);
 
@@ -47,6 +54,7 @@ struct AttnParams {
   int max_pages;
   float scale_log2;          // scale * log2(e): scores live in the log2 domain
   int max_splits;
+  int skip_decode;            // row kernel: leave q_len == 1 tokens to the decode kernel
   uint32_t *status;
   uint32_t *counters;
   float *part_o;
@@ -59,6 +67,12 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
                              int elem_bytes, uint32_t *status, cudaStream_t stream);
 
 cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t stream);
+
+// Streaming split-KV decode kernel (bf16; head_dim 64/128; GQA group 2/4/8
+// with group * head_dim <= 512).
+bool decode_fast_path(int dtype, int D, int G);
+cudaError_t launch_attention_decode(const AttnParams &p, int grid, cudaStream_t stream);
+int decode_grid(int device);
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -129,6 +129,46 @@ def test_small_hybrid_batches(cuda_device, case):
     assert_close(out.cpu(), want, f"case {case}")
 
 
+DECODE_CASES = [
+    # (num decodes, ctx range, Hq, Hkv, D) -- decode kernel shapes and fallbacks
+    (3, (1, 40), 8, 4, 128),       # fewer pages than workers, ragged pages
+    (40, (1, 700), 32, 8, 128),
+    (17, (100, 3000), 16, 8, 128),  # G = 2
+    (9, (1, 2000), 32, 4, 64),      # G = 8, D = 64
+    (25, (30, 1500), 16, 4, 64),    # G = 4, D = 64
+    (11, (500, 900), 8, 4, 64),     # G = 2, D = 64
+    (7, (1, 1000), 64, 8, 128),     # G = 8, D = 128: row kernel
+    (5, (1, 600), 8, 8, 128),       # G = 1: row kernel
+]
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_CASES)))
+def test_decode_batches(cuda_device, case):
+    n, (lo, hi), Hq, Hkv, D = DECODE_CASES[case]
+    g = torch.Generator().manual_seed(500 + case)
+    seq_lens = torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+    # one chunk too, so both roles run in the same call
+    q_lens = [1] * n + [37]
+    seq_lens = seq_lens + [37 + 50]
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=600 + case)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(D)
+    out, wsp = gpu_step(k_cache, v_cache, inp, scale, Hq)
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    assert_close(out.cpu(), want, f"decode case {case}")
+    assert ops.device_status(k_cache, Hq, m.block_table.shape[1], wsp) == 0
+    # a second call on the same workspace (counters were reset) gives the same bits
+    out2 = ops.attention_forward(inp["q"], k_cache, v_cache, inp["meta"].block_table,
+                                 inp["meta"].query_start_loc, inp["meta"].seq_lens, scale, wsp)
+    assert torch.equal(bits(out), bits(out2))
+
+
 def test_ones_values_give_ones_and_onehot_values_give_probabilities(cuda_device):
     """V == 1 makes every output 1 (softmax rows sum to 1, including across
     merged splits); V_j = e_j (ctx <= D) makes the output row the probability

@@ -56,10 +56,10 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, name):
 
 
 def test_noalloc_rejects_steps_beyond_its_scratch(cuda_device):
-    # 256 decodes of up to 8192 keys need more split scratch than the fixed array
+    # 1024 sequences need more split-KV scratch than the fixed array holds
     k_cache = torch.empty(4, 8, 16, 128, dtype=torch.bfloat16, device=cuda_device)
-    desc = ops.make_desc(k_cache, 32, 256, 512)
-    assert ops.cpa_workspace_bytes(desc, 256) > ops.CPA_NOALLOC_SCRATCH_BYTES
+    desc = ops.make_desc(k_cache, 32, 1024, 512)
+    assert ops.cpa_workspace_bytes(desc, 1024) > ops.CPA_NOALLOC_SCRATCH_BYTES
     P = ctypes.c_void_p(k_cache.data_ptr())
-    rc = ops.cpa_attention_forward_noalloc(P, P, P, P, P, P, 256, 0.1, P, None, desc)
+    rc = ops.cpa_attention_forward_noalloc(P, P, P, P, P, P, 1024, 0.1, P, None, desc)
     assert rc == ops.CPA_ERR_WORKSPACE
