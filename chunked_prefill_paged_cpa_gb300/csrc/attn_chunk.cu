@@ -1,0 +1,484 @@
+// Prefill-chunk attention on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// A chunk of q_len new tokens attends to everything its sequence already has
+// in the paged cache plus a causal mask inside the chunk ("vllm-learning-book
+// 05. Chunked Prefill", section 3; "Chunked Prefill 技术深度解析", section 4.1;
+// "How Chunked Prefill Stops Decode Starvation", "The fix").  That is a dense
+// contraction: one CTA computes one 128-row tile against every visible key.
+//
+// Tile rows (BM = 128) pack the G query heads that share kv head g (GQA):
+// row r = (token m*TM + r/G of the chunk, head g*G + r%G), TM = 128/G tokens.
+// Each K/V byte read from the paged cache therefore serves all G heads.
+//
+// Per CTA (192 threads, one CTA per SM):
+//   warp 0     TMA producer: the Q tile once (3-d tensor map, 128-byte
+//              swizzle), then per KV tile of BN = 128 keys the 8 pages of K
+//              and of V for kv head g (2-d tensor map over the cache rows);
+//              pages past the sequence are loaded from an out-of-range row
+//              and arrive as zeros.  Two K/V stages.
+//   warp 1     allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
+//              S_j = Q K_j^T into one of two TMEM S buffers, and
+//              O += P_{j-1} V_{j-1} (P from shared memory, V MN-major),
+//              so QK^T of tile j overlaps the softmax of tile j-1.
+//   warps 2-5  softmax, one thread per row: load S from TMEM, causal mask,
+//              online max in the log2 domain with lazy rescaling of the TMEM
+//              O accumulator (only when the running max grows by more than
+//              2^8), exp2, row sum, P in bf16 to shared memory (128-byte
+//              swizzled, K-major), and at the end O / l to global memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "cpa_internal.cuh"
+#include "ptx.cuh"
+
+namespace cpa {
+namespace {
+
+constexpr int kPage = 16;
+constexpr int BM = 128;          // tile rows
+constexpr int BN = 128;          // keys per KV tile (8 pages)
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct ChunkCfg {
+  static constexpr int PANELS = D / 64;          // 128-byte swizzle panels along head_dim
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;    // one K (or V) tile
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers, scan scratch, 1 KB alignment
+};
+
+struct Bars {
+  uint64_t q, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], p_free[2];
+  uint32_t tmem_base;
+  int tile_s, tile_li, tile_total;
+  int warp_sum[kThreads / 32];
+};
+
+__device__ __forceinline__ int seq_tiles(const AttnParams &p, int s, int G) {
+  const int q_len = __ldg(p.query_start_loc + s + 1) - __ldg(p.query_start_loc + s);
+  if (q_len < 2) return 0;
+  return p.Hkv * ((q_len * G + BM - 1) / BM);
+}
+
+// Find which (sequence, local tile) this CTA owns; all threads participate.
+__device__ void find_tile(const AttnParams &p, int G, int tile_id, Bars *bs) {
+  const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (S + kThreads - 1) / kThreads;
+  const int s0 = tid * per, s1 = min(S, s0 + per);
+  int local = 0;
+  for (int s = s0; s < s1; ++s) local += seq_tiles(p, s, G);
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (tid == 0) bs->tile_s = -1;
+  if (lane == 31) bs->warp_sum[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) base += bs->warp_sum[w];
+    total += bs->warp_sum[w];
+  }
+  incl += base;
+  const int excl = incl - local;
+  if (tile_id >= excl && tile_id < incl) {
+    int acc = excl;
+    for (int s = s0; s < s1; ++s) {
+      const int c = seq_tiles(p, s, G);
+      if (tile_id < acc + c) {
+        bs->tile_s = s;
+        bs->tile_li = tile_id - acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  if (tid == 0) bs->tile_total = total;
+  __syncthreads();
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, int kv_rows) {
+  using C = ChunkCfg<D>;
+  constexpr int TM = BM / G;  // tokens per tile
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char *sQ = smem + C::OFF_Q;
+  unsigned char *sK = smem + C::OFF_K;
+  unsigned char *sV = smem + C::OFF_V;
+  unsigned char *sP = smem + C::OFF_P;
+  Bars *bs = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  find_tile(p, G, blockIdx.x, bs);
+  if (bs->tile_s < 0) return;  // uniform: more CTAs than tiles
+  const int s = bs->tile_s;
+  const int mt = ((__ldg(p.query_start_loc + s + 1) - __ldg(p.query_start_loc + s)) * G + BM - 1) / BM;
+  const int g = bs->tile_li % p.Hkv;
+  const int m = mt - 1 - bs->tile_li / p.Hkv;  // later tiles (more keys) first
+  const int qs = __ldg(p.query_start_loc + s);
+  const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
+  int ctx = __ldg(p.seq_lens + s);
+  const int cap = p.max_pages * kPage;
+  if (ctx > cap) ctx = cap;
+  if (ctx < q_len) return;  // malformed; the host contract forbids it
+  const int t0 = qs + m * TM;
+  const int last_tok = min(m * TM + TM - 1, q_len - 1);  // last valid chunk index of the tile
+  const int max_last = ctx - q_len + last_tok;
+  const int n_kv = max_last / BN + 1;
+  const int n_pages = (ctx + kPage - 1) / kPage;
+
+  if (tid == 0) {
+    ptx::mbar_init(&bs->q, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bs->k_full[i], 1);
+      ptx::mbar_init(&bs->v_full[i], 1);
+      ptx::mbar_init(&bs->kv_empty[i], 1);
+      ptx::mbar_init(&bs->s_full[i], 1);
+      ptx::mbar_init(&bs->p_full[i], 128);
+      ptx::mbar_init(&bs->p_free[i], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(&bs->tmem_base, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = bs->tmem_base;
+  const uint32_t tO = tmem + 256;  // S buffers at columns [0, 128) and [128, 256)
+
+  if (warp == 0) {
+    // ------------------------------- TMA producer -------------------------------
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm_q);
+      ptx::prefetch_tmap(&tm_k);
+      ptx::prefetch_tmap(&tm_v);
+      ptx::mbar_arrive_expect_tx(&bs->q, C::Q_BYTES);
+#pragma unroll
+      for (int pl = 0; pl < C::PANELS; ++pl)
+        ptx::tma_load_3d(sQ + pl * BM * 128, &tm_q, pl * 64, g * G, t0, &bs->q);
+    }
+    const int32_t *bt = p.block_table + (int64_t)s * p.max_pages;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      if (j >= 2 && !ptx::mbar_wait(&bs->kv_empty[st], ((j - 2) >> 1) & 1)) {
+        if (lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
+        break;
+      }
+      int row = kv_rows;  // out of range: zero fill
+      if (lane < 8) {
+        const int pi = j * 8 + lane;
+        if (pi < n_pages) {
+          const int page = __ldg(bt + pi);
+          if (page >= 0 && page < p.num_pages) {
+            row = (page * p.Hkv + g) * kPage;
+          } else {
+            atomicOr(p.status, STATUS_BAD_PAGE);
+          }
+        }
+      }
+      int rows[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, row, i);
+      if (lane == 0) {
+        unsigned char *dk = sK + st * C::KV_BYTES;
+        unsigned char *dv = sV + st * C::KV_BYTES;
+        ptx::mbar_arrive_expect_tx(&bs->k_full[st], C::KV_BYTES);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int pl = 0; pl < C::PANELS; ++pl)
+            ptx::tma_load_2d(dk + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i],
+                             &bs->k_full[st]);
+        ptx::mbar_arrive_expect_tx(&bs->v_full[st], C::KV_BYTES);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int pl = 0; pl < C::PANELS; ++pl)
+            ptx::tma_load_2d(dv + pl * BN * 128 + i * kPage * 128, &tm_v, pl * 64, rows[i],
+                             &bs->v_full[st]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------- MMA issuer ---------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
+      bool ok = ptx::mbar_wait(&bs->q, 0);
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i & 1;
+        const uint32_t par = (i >> 1) & 1;
+        if (!ptx::mbar_wait(&bs->p_full[st], par) || !ptx::mbar_wait(&bs->v_full[st], par))
+          return false;
+        ptx::tc_fence_after();
+        const unsigned char *pp = sP + st * C::P_BYTES;
+        const unsigned char *vv = sV + st * C::KV_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint64_t a = ptx::smem_desc_sw128(pp + (ks >> 2) * BM * 128 + (ks & 3) * 32, 16,
+                                                  1024);
+          const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
+          ptx::mma_bf16_ss(tO, a, b, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(&bs->p_free[st]);
+        ptx::mma_commit(&bs->kv_empty[st]);
+        return true;
+      };
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j & 1;
+        if (!ptx::mbar_wait(&bs->k_full[st], (j >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const unsigned char *kk = sK + st * C::KV_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int pl = ks >> 2, within = (ks & 3) * 32;
+          const uint64_t a = ptx::smem_desc_sw128(sQ + pl * BM * 128 + within, 16, 1024);
+          const uint64_t b = ptx::smem_desc_sw128(kk + pl * BN * 128 + within, 16, 1024);
+          ptx::mma_bf16_ss(tmem + st * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&bs->s_full[st]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) ok = issue_pv(n_kv - 1);
+      if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
+    }
+  } else {
+    // ------------------------------- softmax ------------------------------------
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;        // tile row
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int tok = m * TM + r / G;           // index within the chunk
+    const bool row_valid = tok < q_len;
+    const int last = row_valid ? ctx - q_len + tok : 0;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (!ptx::mbar_wait(&bs->s_full[st], par)) { ok = false; break; }
+      ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tmem + st * 128 + lane_off + c * 32, sr[c]);
+      ptx::tmem_wait_ld();
+      const int key0 = j * BN;
+      const bool need_mask = key0 + BN - 1 > last;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float v = __uint_as_float(sr[c][e]);
+          if (need_mask && key0 + c * 32 + e > last) v = -INFINITY;
+          sr[c][e] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      const float mnew = fmaxf(m_run, mx * p.scale_log2);
+      if (j == 0) {
+        m_run = mnew;
+      } else {
+        // Rescale the O accumulator only when a row's running max grew by more
+        // than the threshold (PV_{j-1} must have completed).  TMEM loads and
+        // stores are warp-collective, so the whole warp takes the branch if any
+        // of its rows needs it; the other rows multiply by 1.
+        const bool need = mnew > m_run + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? exp2f(m_run - mnew) : 1.f;
+          if (!ptx::mbar_wait(&bs->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + lane_off + c * 32, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(tO + lane_off + c * 32, o);
+          }
+          ptx::tmem_wait_st();
+          if (need) {
+            l_run *= alpha;
+            m_run = mnew;
+          }
+        }
+      }
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+      // P[st] is free once PV_{j-2} has completed
+      if (j >= 2 && !ptx::mbar_wait(&bs->p_free[st], ((j - 2) >> 1) & 1)) { ok = false; break; }
+      unsigned char *prow = sP + st * C::P_BYTES + r * 128;
+      float rs = 0.f;
+#pragma unroll
+      for (int q8 = 0; q8 < 16; ++q8) {  // 16 chunks of 8 keys
+        uint32_t wds[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int c = q8 >> 2, e = (q8 & 3) * 8 + h * 2;
+          const float p0 = exp2f(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, -mref));
+          const float p1 = exp2f(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, -mref));
+          rs += p0 + p1;
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          wds[h] = *reinterpret_cast<uint32_t *>(&b2);
+        }
+        const int panel = q8 >> 3, cpos = (q8 & 7) ^ (r & 7);
+        *reinterpret_cast<uint4 *>(prow + panel * BM * 128 + cpos * 16) =
+            make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      }
+      l_run += rs;
+      // keys at or past ctx in the last valid page may hold anything: zero those V rows
+      if (key0 + BN > ctx) {
+        if (!ptx::mbar_wait(&bs->v_full[st], par)) { ok = false; break; }
+        const int first_bad = ctx - key0;  // rows >= first_bad of this tile
+        if (r >= first_bad && r < min(BN, n_pages * kPage - key0)) {
+          unsigned char *vrow = sV + st * C::KV_BYTES + r * 128;
+#pragma unroll
+          for (int pl = 0; pl < C::PANELS; ++pl)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4 *>(vrow + pl * BN * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&bs->p_full[st]);
+    }
+    // epilogue: O / l
+    const int nl = n_kv - 1;
+    if (ok && ptx::mbar_wait(&bs->p_free[nl & 1], (nl >> 1) & 1)) {
+      ptx::tc_fence_after();
+      const float inv = 1.f / l_run;
+      __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
+                           ((int64_t)(t0 + r / G) * p.Hq + g * G + r % G) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO + lane_off + c * 32, o);
+        ptx::tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t wds[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[q4 * 8 + h * 2]) * inv,
+                                                        __uint_as_float(o[q4 * 8 + h * 2 + 1]) * inv);
+              wds[h] = *reinterpret_cast<uint32_t *>(&b2);
+            }
+            *reinterpret_cast<uint4 *>(out + c * 32 + q4 * 8) =
+                make_uint4(wds[0], wds[1], wds[2], wds[3]);
+          }
+        }
+      }
+    } else {
+      atomicOr(p.status, STATUS_TIMEOUT);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const AttnParams &p, cudaStream_t stream) {
+  using C = ChunkCfg<D>;
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tq, tk, tv;
+  // q viewed as [T][Hq][D]: box = 64 dims x G heads x BM/G tokens
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.num_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.q), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int64_t rows = p.num_pages * p.Hkv * kPage;
+  for (int which = 0; which < 2; ++which) {
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    cuuint32_t estr[2] = {1, 1};
+    if (encode(which == 0 ? &tk : &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(which == 0 ? p.k_cache : p.v_cache), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  // upper bound on tiles: every chunk adds at most one partial tile per kv head
+  const int64_t grid = (int64_t)p.Hkv * (((int64_t)p.num_tokens * G + BM - 1) / BM + p.num_seqs);
+  attn_chunk_kernel<D, G><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv,
+                                                                        (int)rows);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_tc_path(int dtype, int D, int G) {
+  if (dtype != CPA_BF16) return false;
+  if (D != 64 && D != 128) return false;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaError_t launch_attention_chunk(const AttnParams &p, cudaStream_t stream) {
+  const int G = p.Hq / p.Hkv;
+  if (p.D == 128) {
+    switch (G) {
+      case 1: return launch_dg<128, 1>(p, stream);
+      case 2: return launch_dg<128, 2>(p, stream);
+      case 4: return launch_dg<128, 4>(p, stream);
+      case 8: return launch_dg<128, 8>(p, stream);
+    }
+  } else {
+    switch (G) {
+      case 1: return launch_dg<64, 1>(p, stream);
+      case 2: return launch_dg<64, 2>(p, stream);
+      case 4: return launch_dg<64, 4>(p, stream);
+      case 8: return launch_dg<64, 8>(p, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cpa

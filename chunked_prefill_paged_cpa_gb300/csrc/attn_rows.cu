@@ -73,7 +73,7 @@ attn_rows_kernel(const AttnParams p) {
   const int qs = __ldg(p.query_start_loc + s);
   const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
   if (t - qs >= q_len) return;  // token past query_start_loc[num_seqs]: not owned
-  if (q_len == 1 && p.skip_decode) return;
+  if ((q_len == 1 && p.rows_mode == 1) || (q_len > 1 && p.rows_mode == 2)) return;
   int ctx = __ldg(p.seq_lens + s);
   const int cap = p.max_pages * p.page_size;
   if (ctx > cap) {  // contract violation: never read past the block table row
@@ -207,7 +207,7 @@ attn_rows_kernel(const AttnParams p) {
 
 template <typename Elem, int D>
 cudaError_t launch_d(const AttnParams &p, cudaStream_t stream) {
-  const dim3 grid(p.num_tokens, p.Hkv, p.skip_decode ? 1 : p.max_splits);
+  const dim3 grid(p.num_tokens, p.Hkv, p.rows_mode == 1 ? 1 : p.max_splits);
   switch (p.Hq / p.Hkv) {
     case 1: attn_rows_kernel<Elem, D, 1><<<grid, kWarps * 32, 0, stream>>>(p); break;
     case 2: attn_rows_kernel<Elem, D, 2><<<grid, kWarps * 32, 0, stream>>>(p); break;

@@ -152,6 +152,12 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
   p.part_o = reinterpret_cast<float *>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
   cudaStream_t st = (cudaStream_t)stream;
+  const int G = p.Hq / p.Hkv;
+  const bool all_decode = (p.num_tokens == num_seqs);  // every q_len is 1
+  const bool tc_chunks = chunk_tc_path(desc->dtype, p.D, G);
+  if (tc_chunks && (int64_t)p.num_pages * p.Hkv * p.page_size >= INT32_MAX)
+    return CPA_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
+  bool rows_for_decodes = true, rows_for_chunks = !all_decode;
   if (w.fast_decode) {
     if (num_seqs > kDecodeMaxSeqs) return CPA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
@@ -160,11 +166,15 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
     int grid = decode_grid(dev);
     if (grid <= 0) return CPA_ERR_CUDA;
     if (grid * 8 > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / 8;
-    cudaError_t e = launch_attention_decode(p, grid, st);
-    if (e != cudaSuccess) return CPA_ERR_CUDA;
-    if (p.num_tokens == num_seqs) return CPA_OK;  // every sequence is a decode
-    p.skip_decode = 1;
+    if (launch_attention_decode(p, grid, st) != cudaSuccess) return CPA_ERR_CUDA;
+    rows_for_decodes = false;
   }
+  if (tc_chunks && !all_decode) {
+    if (launch_attention_chunk(p, st) != cudaSuccess) return CPA_ERR_CUDA;
+    rows_for_chunks = false;
+  }
+  if (!rows_for_decodes && !rows_for_chunks) return CPA_OK;
+  p.rows_mode = (rows_for_decodes && rows_for_chunks) ? 0 : (rows_for_chunks ? 1 : 2);
   cudaError_t e = launch_attention_rows(p, desc->dtype, st);
   return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }

@@ -54,7 +54,7 @@ struct AttnParams {
   int max_pages;
   float scale_log2;          // scale * log2(e): scores live in the log2 domain
   int max_splits;
-  int skip_decode;            // row kernel: leave q_len == 1 tokens to the decode kernel
+  int rows_mode;              // row kernel: 0 all tokens, 1 only q_len > 1, 2 only q_len == 1
   uint32_t *status;
   uint32_t *counters;
   float *part_o;
@@ -73,6 +73,10 @@ cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t s
 bool decode_fast_path(int dtype, int D, int G);
 cudaError_t launch_attention_decode(const AttnParams &p, int grid, cudaStream_t stream);
 int decode_grid(int device);
+
+// Prefill-chunk tiles on tcgen05 (bf16; head_dim 64/128; GQA group 1/2/4/8).
+bool chunk_tc_path(int dtype, int D, int G);
+cudaError_t launch_attention_chunk(const AttnParams &p, cudaStream_t stream);
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
