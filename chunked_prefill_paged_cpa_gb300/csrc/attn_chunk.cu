@@ -4,27 +4,30 @@
 // in the paged cache plus a causal mask inside the chunk ("vllm-learning-book
 // 05. Chunked Prefill", section 3; "Chunked Prefill 技术深度解析", section 4.1;
 // "How Chunked Prefill Stops Decode Starvation", "The fix").  That is a dense
-// contraction: one CTA computes one 128-row tile against every visible key.
+// contraction: one CTA computes two 128-row query tiles against every key
+// they can see.
 //
 // Tile rows (BM = 128) pack the G query heads that share kv head g (GQA):
 // row r = (token m*TM + r/G of the chunk, head g*G + r%G), TM = 128/G tokens.
-// Each K/V byte read from the paged cache therefore serves all G heads.
+// Each K/V byte read from the paged cache therefore serves all G heads, and
+// the two tiles of a CTA (m = 2mp, 2mp+1) share every K/V tile.
 //
-// Per CTA (192 threads, one CTA per SM):
-//   warp 0     TMA producer: the Q tile once (3-d tensor map, 128-byte
+// Per CTA (320 threads, one CTA per SM):
+//   warps 0-3  softmax for tile 0, warps 4-7 softmax for tile 1; one thread
+//              per row.  Load S from TMEM, causal mask (diagonal tiles only),
+//              running max in the log2 domain with lazy rescaling of the TMEM
+//              O accumulator (only when the max grows by more than 2^8), exp2,
+//              row sum, and P in bf16 written back into TMEM over S.
+//   warp 8     TMA producer: both Q tiles (3-d tensor map over q, 128-byte
 //              swizzle), then per KV tile of BN = 128 keys the 8 pages of K
-//              and of V for kv head g (2-d tensor map over the cache rows);
-//              pages past the sequence are loaded from an out-of-range row
-//              and arrive as zeros.  Two K/V stages.
-//   warp 1     allocates 512 TMEM columns; lane 0 issues every tcgen05.mma:
-//              S_j = Q K_j^T into one of two TMEM S buffers, and
-//              O += P_{j-1} V_{j-1} (P from shared memory, V MN-major),
-//              so QK^T of tile j overlaps the softmax of tile j-1.
-//   warps 2-5  softmax, one thread per row: load S from TMEM, causal mask,
-//              online max in the log2 domain with lazy rescaling of the TMEM
-//              O accumulator (only when the running max grows by more than
-//              2^8), exp2, row sum, P in bf16 to shared memory (128-byte
-//              swizzled, K-major), and at the end O / l to global memory.
+//              and of V of kv head g (2-d tensor map over the cache rows);
+//              pages past the sequence are read from an out-of-range row and
+//              arrive as zeros.  Two K/V stages.
+//   warp 9     allocates the 512 TMEM columns (S0, S1, O0, O1); lane 0 issues
+//              every tcgen05.mma: S_i = Q_i K_j^T (both operands from shared
+//              memory) and O_i += P_i V_j (P from TMEM, V MN-major in shared
+//              memory).  The two tiles ping-pong: while one warpgroup runs its
+//              softmax, the tensor core runs the other tile's PV and next QK^T.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,45 +38,45 @@ namespace cpa {
 namespace {
 
 constexpr int kPage = 16;
-constexpr int BM = 128;          // tile rows
+constexpr int BM = 128;          // rows per query tile
 constexpr int BN = 128;          // keys per KV tile (8 pages)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct ChunkCfg {
   static constexpr int PANELS = D / 64;          // 128-byte swizzle panels along head_dim
-  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int Q_BYTES = BM * D * 2;     // one query tile
   static constexpr int KV_BYTES = BN * D * 2;    // one K (or V) tile
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_Q = 0;                // two query tiles
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers, scan scratch, 1 KB alignment
 };
 
 struct Bars {
-  uint64_t q, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], p_free[2];
+  uint64_t q, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_final[2];
   uint32_t tmem_base;
   int tile_s, tile_li, tile_total;
   int warp_sum[kThreads / 32];
 };
 
-__device__ __forceinline__ int seq_tiles(const AttnParams &p, int s, int G) {
+__device__ __forceinline__ int seq_work(const AttnParams &p, int s, int G) {
   const int q_len = __ldg(p.query_start_loc + s + 1) - __ldg(p.query_start_loc + s);
   if (q_len < 2) return 0;
-  return p.Hkv * ((q_len * G + BM - 1) / BM);
+  const int mt = (q_len * G + BM - 1) / BM;
+  return p.Hkv * ((mt + 1) / 2);
 }
 
-// Find which (sequence, local tile) this CTA owns; all threads participate.
+// Find which (sequence, local work item) this CTA owns; all threads participate.
 __device__ void find_tile(const AttnParams &p, int G, int tile_id, Bars *bs) {
   const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (S + kThreads - 1) / kThreads;
   const int s0 = tid * per, s1 = min(S, s0 + per);
   int local = 0;
-  for (int s = s0; s < s1; ++s) local += seq_tiles(p, s, G);
+  for (int s = s0; s < s1; ++s) local += seq_work(p, s, G);
   int incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -93,7 +96,7 @@ __device__ void find_tile(const AttnParams &p, int G, int tile_id, Bars *bs) {
   if (tile_id >= excl && tile_id < incl) {
     int acc = excl;
     for (int s = s0; s < s1; ++s) {
-      const int c = seq_tiles(p, s, G);
+      const int c = seq_work(p, s, G);
       if (tile_id < acc + c) {
         bs->tile_s = s;
         bs->tile_li = tile_id - acc;
@@ -119,26 +122,35 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
   unsigned char *sQ = smem + C::OFF_Q;
   unsigned char *sK = smem + C::OFF_K;
   unsigned char *sV = smem + C::OFF_V;
-  unsigned char *sP = smem + C::OFF_P;
   Bars *bs = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   find_tile(p, G, blockIdx.x, bs);
-  if (bs->tile_s < 0) return;  // uniform: more CTAs than tiles
+  if (bs->tile_s < 0) return;  // uniform: more CTAs than work items
   const int s = bs->tile_s;
-  const int mt = ((__ldg(p.query_start_loc + s + 1) - __ldg(p.query_start_loc + s)) * G + BM - 1) / BM;
-  const int g = bs->tile_li % p.Hkv;
-  const int m = mt - 1 - bs->tile_li / p.Hkv;  // later tiles (more keys) first
   const int qs = __ldg(p.query_start_loc + s);
   const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
+  const int mt = (q_len * G + BM - 1) / BM;
+  const int npair = (mt + 1) / 2;
+  const int g = bs->tile_li % p.Hkv;
+  const int mp = npair - 1 - bs->tile_li / p.Hkv;  // later tiles (more keys) first
   int ctx = __ldg(p.seq_lens + s);
   const int cap = p.max_pages * kPage;
   if (ctx > cap) ctx = cap;
   if (ctx < q_len) return;  // malformed; the host contract forbids it
-  const int t0 = qs + m * TM;
-  const int last_tok = min(m * TM + TM - 1, q_len - 1);  // last valid chunk index of the tile
-  const int max_last = ctx - q_len + last_tok;
-  const int n_kv = max_last / BN + 1;
+  // the two query tiles of this CTA and the KV tiles each must visit
+  int n_kv_t[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int m = 2 * mp + i;
+    if (m < mt) {
+      const int last_tok = min(m * TM + TM - 1, q_len - 1);
+      n_kv_t[i] = (ctx - q_len + last_tok) / BN + 1;
+    } else {
+      n_kv_t[i] = 0;
+    }
+  }
+  const int n_kv = max(n_kv_t[0], n_kv_t[1]);
   const int n_pages = (ctx + kPage - 1) / kPage;
 
   if (tid == 0) {
@@ -149,27 +161,29 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_init(&bs->kv_empty[i], 1);
       ptx::mbar_init(&bs->s_full[i], 1);
       ptx::mbar_init(&bs->p_full[i], 128);
-      ptx::mbar_init(&bs->p_free[i], 1);
+      ptx::mbar_init(&bs->o_final[i], 1);
     }
     ptx::fence_mbar_init();
   }
-  if (warp == 1) ptx::tmem_alloc(&bs->tmem_base, 512);
+  if (warp == kMmaWarp) ptx::tmem_alloc(&bs->tmem_base, 512);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = bs->tmem_base;
-  const uint32_t tO = tmem + 256;  // S buffers at columns [0, 128) and [128, 256)
+  const uint32_t tmem = bs->tmem_base;  // S_i at columns 128*i, O_i at 256 + 128*i
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------- TMA producer -------------------------------
     if (lane == 0) {
       ptx::prefetch_tmap(&tm_q);
       ptx::prefetch_tmap(&tm_k);
       ptx::prefetch_tmap(&tm_v);
-      ptx::mbar_arrive_expect_tx(&bs->q, C::Q_BYTES);
+      const int ntiles = n_kv_t[1] > 0 ? 2 : 1;
+      ptx::mbar_arrive_expect_tx(&bs->q, ntiles * C::Q_BYTES);
+      for (int i = 0; i < ntiles; ++i)
 #pragma unroll
-      for (int pl = 0; pl < C::PANELS; ++pl)
-        ptx::tma_load_3d(sQ + pl * BM * 128, &tm_q, pl * 64, g * G, t0, &bs->q);
+        for (int pl = 0; pl < C::PANELS; ++pl)
+          ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, g * G,
+                           qs + (2 * mp + i) * TM, &bs->q);
     }
     const int32_t *bt = p.block_table + (int64_t)s * p.max_pages;
     for (int j = 0; j < n_kv; ++j) {
@@ -212,136 +226,167 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                              &bs->v_full[st]);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------- MMA issuer ---------------------------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
-      bool ok = ptx::mbar_wait(&bs->q, 0);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        const uint32_t par = (i >> 1) & 1;
-        if (!ptx::mbar_wait(&bs->p_full[st], par) || !ptx::mbar_wait(&bs->v_full[st], par))
-          return false;
-        ptx::tc_fence_after();
-        const unsigned char *pp = sP + st * C::P_BYTES;
-        const unsigned char *vv = sV + st * C::KV_BYTES;
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t a = ptx::smem_desc_sw128(pp + (ks >> 2) * BM * 128 + (ks & 3) * 32, 16,
-                                                  1024);
-          const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
-          ptx::mma_bf16_ss(tO, a, b, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        ptx::mma_commit(&bs->p_free[st]);
-        ptx::mma_commit(&bs->kv_empty[st]);
-        return true;
-      };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!ptx::mbar_wait(&bs->k_full[st], (j >> 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const unsigned char *kk = sK + st * C::KV_BYTES;
+      auto issue_qk = [&](int i, int j) {
+        const unsigned char *kk = sK + (j & 1) * C::KV_BYTES;
+        const unsigned char *qq = sQ + i * C::Q_BYTES;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int pl = ks >> 2, within = (ks & 3) * 32;
-          const uint64_t a = ptx::smem_desc_sw128(sQ + pl * BM * 128 + within, 16, 1024);
+          const uint64_t a = ptx::smem_desc_sw128(qq + pl * BM * 128 + within, 16, 1024);
           const uint64_t b = ptx::smem_desc_sw128(kk + pl * BN * 128 + within, 16, 1024);
-          ptx::mma_bf16_ss(tmem + st * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(tmem + i * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&bs->s_full[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        ptx::mma_commit(&bs->s_full[i]);
+      };
+      bool ok = ptx::mbar_wait(&bs->q, 0) && ptx::mbar_wait(&bs->k_full[0], 0);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_qk(0, 0);
+        if (n_kv_t[1] > 0) issue_qk(1, 0);
       }
-      if (ok) ok = issue_pv(n_kv - 1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j & 1;
+        bool v_ready = false, k_next_ready = false;
+        for (int i = 0; ok && i < 2; ++i) {
+          const int n_i = i ? n_kv_t[1] : n_kv_t[0];
+          if (j >= n_i) continue;
+          if (!ptx::mbar_wait(&bs->p_full[i], j & 1)) { ok = false; break; }
+          if (!v_ready) {
+            if (!ptx::mbar_wait(&bs->v_full[st], (j >> 1) & 1)) { ok = false; break; }
+            v_ready = true;
+          }
+          ptx::tc_fence_after();
+          const unsigned char *vv = sV + st * C::KV_BYTES;
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
+            ptx::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, b, idesc_pv,
+                             (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (j + 1 < n_i) {
+            if (!k_next_ready) {
+              if (!ptx::mbar_wait(&bs->k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) { ok = false; break; }
+              k_next_ready = true;
+              ptx::tc_fence_after();
+            }
+            issue_qk(i, j + 1);
+          } else {
+            ptx::mma_commit(&bs->o_final[i]);
+          }
+        }
+        ptx::mma_commit(&bs->kv_empty[st]);
+      }
       if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
     }
   } else {
     // ------------------------------- softmax ------------------------------------
+    const int ti = warp >> 2;                 // query tile of this warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;        // tile row
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + ti * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + ti * 128 + lane_off;
+    const int m = 2 * mp + ti;
+    const int n_mine = ti ? n_kv_t[1] : n_kv_t[0];
     const int tok = m * TM + r / G;           // index within the chunk
     const bool row_valid = tok < q_len;
     const int last = row_valid ? ctx - q_len + tok : 0;
+    const float sl2 = p.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      const uint32_t par = (j >> 1) & 1;
-      if (!ptx::mbar_wait(&bs->s_full[st], par)) { ok = false; break; }
+    bool ok = n_mine > 0;
+    for (int j = 0; ok && j < n_mine; ++j) {
+      if (!ptx::mbar_wait(&bs->s_full[ti], j & 1)) { ok = false; break; }
       ptx::tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tmem + st * 128 + lane_off + c * 32, sr[c]);
-      ptx::tmem_wait_ld();
+      // pass 1: row max over this tile's visible keys, 32 columns at a time
       const int key0 = j * BN;
-      const bool need_mask = key0 + BN - 1 > last;
+      const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
+      const int nvis = last - key0 + 1;        // visible keys of this row in the tile
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        ptx::tmem_ld32(tS + c * 32, sr);
+        ptx::tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float v = __uint_as_float(sr[c][e]);
-          if (need_mask && key0 + c * 32 + e > last) v = -INFINITY;
-          sr[c][e] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
         }
-      const float mnew = fmaxf(m_run, mx * p.scale_log2);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          mx = ptx::max3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+      }
+      const float mnew = fmaxf(m_run, mx * sl2);
       if (j == 0) {
         m_run = mnew;
       } else {
-        // Rescale the O accumulator only when a row's running max grew by more
-        // than the threshold (PV_{j-1} must have completed).  TMEM loads and
-        // stores are warp-collective, so the whole warp takes the branch if any
-        // of its rows needs it; the other rows multiply by 1.
+        // Rescale O only when a row's running max grew by more than the
+        // threshold.  TMEM loads/stores are warp-collective, so the whole warp
+        // takes the branch if any of its rows needs it (the others scale by 1).
+        // S_j being complete implies PV_{j-1} has completed (same issuing
+        // thread, in order), so O is current.
         const bool need = mnew > m_run + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? exp2f(m_run - mnew) : 1.f;
-          if (!ptx::mbar_wait(&bs->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1)) { ok = false; break; }
-          ptx::tc_fence_after();
+          const float alpha = need ? ptx::ex2(m_run - mnew) : 1.f;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            ptx::tmem_ld32(tO + lane_off + c * 32, o);
+            ptx::tmem_ld32(tO + c * 32, o);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st32(tO + lane_off + c * 32, o);
+            ptx::tmem_st32(tO + c * 32, o);
           }
-          ptx::tmem_wait_st();
           if (need) {
             l_run *= alpha;
             m_run = mnew;
           }
         }
       }
+      // pass 2: P = exp2(S * scale - m) in bf16, written over S.  P chunk c
+      // (columns [16c, 16c + 16)) only overwrites S columns already consumed.
       const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-      // P[st] is free once PV_{j-2} has completed
-      if (j >= 2 && !ptx::mbar_wait(&bs->p_free[st], ((j - 2) >> 1) & 1)) { ok = false; break; }
-      unsigned char *prow = sP + st * C::P_BYTES + r * 128;
-      float rs = 0.f;
+      const uint64_t sc2 = ptx::pack2(sl2, sl2);
+      const uint64_t nm2 = ptx::pack2(-mref, -mref);
+      uint64_t rs2 = 0ull;
 #pragma unroll
-      for (int q8 = 0; q8 < 16; ++q8) {  // 16 chunks of 8 keys
-        uint32_t wds[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], pw[16];
+        ptx::tmem_ld32(tS + c * 32, sr);
+        ptx::tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int c = q8 >> 2, e = (q8 & 3) * 8 + h * 2;
-          const float p0 = exp2f(fmaf(__uint_as_float(sr[c][e]), p.scale_log2, -mref));
-          const float p1 = exp2f(fmaf(__uint_as_float(sr[c][e + 1]), p.scale_log2, -mref));
-          rs += p0 + p1;
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          wds[h] = *reinterpret_cast<uint32_t *>(&b2);
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
         }
-        const int panel = q8 >> 3, cpos = (q8 & 7) ^ (r & 7);
-        *reinterpret_cast<uint4 *>(prow + panel * BM * 128 + cpos * 16) =
-            make_uint4(wds[0], wds[1], wds[2], wds[3]);
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const uint64_t x2 = ptx::ffma2(
+              ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
+          float x0, x1;
+          ptx::unpack2(x2, x0, x1);
+          const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+          rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
+          pw[h] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st16(tS + c * 16, pw);
       }
-      l_run += rs;
-      // keys at or past ctx in the last valid page may hold anything: zero those V rows
+      float rs0, rs1;
+      ptx::unpack2(rs2, rs0, rs1);
+      l_run += rs0 + rs1;
+      // Cache slots at or past ctx in the last page may hold anything (NaN
+      // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
+      // runs.  Both warpgroups may write the same zeros; rows past the last
+      // page were loaded out of range and are zero already.
       if (key0 + BN > ctx) {
-        if (!ptx::mbar_wait(&bs->v_full[st], par)) { ok = false; break; }
-        const int first_bad = ctx - key0;  // rows >= first_bad of this tile
-        if (r >= first_bad && r < min(BN, n_pages * kPage - key0)) {
+        const int st = j & 1;
+        if (!ptx::mbar_wait(&bs->v_full[st], (j >> 1) & 1)) { ok = false; break; }
+        if (r >= ctx - key0 && r < n_pages * kPage - key0) {
           unsigned char *vrow = sV + st * C::KV_BYTES + r * 128;
 #pragma unroll
           for (int pl = 0; pl < C::PANELS; ++pl)
@@ -349,46 +394,44 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             for (int c = 0; c < 8; ++c)
               *reinterpret_cast<uint4 *>(vrow + pl * BN * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
+        ptx::fence_proxy_async_smem();
       }
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&bs->p_full[st]);
+      ptx::mbar_arrive(&bs->p_full[ti]);
     }
     // epilogue: O / l
-    const int nl = n_kv - 1;
-    if (ok && ptx::mbar_wait(&bs->p_free[nl & 1], (nl >> 1) & 1)) {
+    if (ok && ptx::mbar_wait(&bs->o_final[ti], 0)) {
       ptx::tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
-                           ((int64_t)(t0 + r / G) * p.Hq + g * G + r % G) * D;
+                           ((int64_t)(qs + tok) * p.Hq + g * G + r % G) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        ptx::tmem_ld32(tO + lane_off + c * 32, o);
+        ptx::tmem_ld32(tO + c * 32, o);
         ptx::tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint32_t wds[4];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[q4 * 8 + h * 2]) * inv,
-                                                        __uint_as_float(o[q4 * 8 + h * 2 + 1]) * inv);
-              wds[h] = *reinterpret_cast<uint32_t *>(&b2);
-            }
+            for (int h = 0; h < 4; ++h)
+              wds[h] = ptx::pack_bf16x2(__uint_as_float(o[q4 * 8 + h * 2]) * inv,
+                                        __uint_as_float(o[q4 * 8 + h * 2 + 1]) * inv);
             *reinterpret_cast<uint4 *>(out + c * 32 + q4 * 8) =
                 make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
         }
       }
-    } else {
+    } else if (n_mine > 0) {
       atomicOr(p.status, STATUS_TIMEOUT);
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
@@ -446,8 +489,10 @@ cudaError_t launch_dg(const AttnParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  // upper bound on tiles: every chunk adds at most one partial tile per kv head
-  const int64_t grid = (int64_t)p.Hkv * (((int64_t)p.num_tokens * G + BM - 1) / BM + p.num_seqs);
+  // upper bound on work items (pairs of 128-row tiles): every chunk adds at
+  // most one partial pair per kv head
+  const int64_t grid =
+      (int64_t)p.Hkv * (((int64_t)p.num_tokens * G + 2 * BM - 1) / (2 * BM) + p.num_seqs);
   attn_chunk_kernel<D, G><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv,
                                                                         (int)rows);
   return cudaGetLastError();

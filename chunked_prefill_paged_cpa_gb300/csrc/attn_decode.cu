@@ -462,29 +462,52 @@ attn_decode_kernel(const AttnParams p) {
         if (lane == 0) prev = atomicAdd(p.counters + sg, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == (unsigned)(wl - wf)) {
-          // last contributor: merge every contributor's partial
+          // last contributor: merge every contributor's partial.  The
+          // contributors' (max, sum) pairs are spread over the lanes; each lane
+          // then owns D/32 output dims and streams the partial outputs with
+          // independent loads, 8 contributors at a time.
           __threadfence();
+          const int nc = wl - wf + 1;
+          const int64_t base = (int64_t)sg + wf;
           __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
                                ((int64_t)tok * p.Hq + (int64_t)cc.g * G) * D;
           for (int r = 0; r < G; ++r) {
             float mx = -INFINITY;
-            for (int c = wf; c <= wl; ++c)
-              mx = fmaxf(mx, __ldcg(&p.part_ml[((int64_t)sg + c) * G + r].x));
-            float lsum = 0.f, acc[D / 32];
+            for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(&p.part_ml[(base + c) * G + r].x));
 #pragma unroll
-            for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
-            for (int c = wf; c <= wl; ++c) {
-              const float2 ml = __ldcg(&p.part_ml[((int64_t)sg + c) * G + r]);
-              const float sc = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mx);
-              lsum += ml.y * sc;
-              const float *src = p.part_o + (((int64_t)sg + c) * G + r) * D + lane * (D / 32);
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float lsum = 0.f;
+            for (int c = lane; c < nc; c += 32) {
+              const float2 ml = __ldcg(&p.part_ml[(base + c) * G + r]);
+              lsum += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - mx);
+            }
 #pragma unroll
-              for (int e = 0; e < D / 32; ++e) acc[e] += __ldcg(src + e) * sc;
+            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+            constexpr int DPL = D / 32;  // dims per lane
+            float acc[DPL];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+            for (int c0 = 0; c0 < nc; c0 += 8) {
+              float wgt[8];
+              float ov[8][DPL];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int c = min(c0 + u, nc - 1);
+                const float mc = __ldcg(&p.part_ml[(base + c) * G + r].x);
+                wgt[u] = (c0 + u < nc && mc != -INFINITY) ? exp2f(mc - mx) : 0.f;
+                const float *src = p.part_o + ((base + c) * G + r) * D + lane * DPL;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) ov[u][e] = __ldcg(src + e);
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(ov[u][e], wgt[u], acc[e]);
             }
             const float inv = 1.f / lsum;
 #pragma unroll
-            for (int e = 0; e < D / 32; e += 2) {
-              *reinterpret_cast<__nv_bfloat162 *>(out + r * D + lane * (D / 32) + e) =
+            for (int e = 0; e < DPL; e += 2) {
+              *reinterpret_cast<__nv_bfloat162 *>(out + r * D + lane * DPL + e) =
                   __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
             }
           }
