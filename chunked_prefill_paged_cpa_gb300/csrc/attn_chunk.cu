@@ -57,10 +57,8 @@ struct ChunkCfg {
 };
 
 struct Bars {
-  uint64_t q, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_final[2];
+  uint64_t q_full, q_empty, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_final[2];
   uint32_t tmem_base;
-  int tile_s, tile_li, tile_total;
-  int warp_sum[kThreads / 32];
 };
 
 __device__ __forceinline__ int seq_work(const AttnParams &p, int s, int G) {
@@ -70,11 +68,30 @@ __device__ __forceinline__ int seq_work(const AttnParams &p, int s, int G) {
   return p.Hkv * ((mt + 1) / 2);
 }
 
-// Find which (sequence, local work item) this CTA owns; all threads participate.
-__device__ void find_tile(const AttnParams &p, int G, int tile_id, Bars *bs) {
-  const int S = p.num_seqs, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (S + kThreads - 1) / kThreads;
-  const int s0 = tid * per, s1 = min(S, s0 + per);
+// One work item = two consecutive 128-row query tiles (m = 2mp, 2mp+1) of one
+// (chunk sequence, kv head).  Every warp locates its items on its own with a
+// warp-level prefix sum over the sequences, so the warp roles never have to
+// synchronise with each other between items.
+struct Item {
+  int s, qs, q_len, ctx, g, mp, mt, n_kv0, n_kv1, n_kv, n_pages;
+};
+
+__device__ int warp_total_items(const AttnParams &p, int G) {
+  const int lane = threadIdx.x & 31;
+  int local = 0;
+  for (int s = lane; s < p.num_seqs; s += 32) local += seq_work(p, s, G);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+  return local;
+}
+
+template <int G>
+__device__ bool warp_find_item(const AttnParams &p, int item, Item &it) {
+  constexpr int TM = BM / G;
+  const int lane = threadIdx.x & 31;
+  const int S = p.num_seqs;
+  const int per = (S + 31) / 32;
+  const int s0 = lane * per, s1 = min(S, s0 + per);
   int local = 0;
   for (int s = s0; s < s1; ++s) local += seq_work(p, s, G);
   int incl = local;
@@ -83,30 +100,38 @@ __device__ void find_tile(const AttnParams &p, int G, int tile_id, Bars *bs) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += v;
   }
-  if (tid == 0) bs->tile_s = -1;
-  if (lane == 31) bs->warp_sum[warp] = incl;
-  __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
-    if (w < warp) base += bs->warp_sum[w];
-    total += bs->warp_sum[w];
-  }
-  incl += base;
   const int excl = incl - local;
-  if (tile_id >= excl && tile_id < incl) {
+  int fs = -1, fli = 0;
+  if (item >= excl && item < incl) {
     int acc = excl;
     for (int s = s0; s < s1; ++s) {
       const int c = seq_work(p, s, G);
-      if (tile_id < acc + c) {
-        bs->tile_s = s;
-        bs->tile_li = tile_id - acc;
-        break;
-      }
+      if (item < acc + c) { fs = s; fli = item - acc; break; }
       acc += c;
     }
   }
-  if (tid == 0) bs->tile_total = total;
-  __syncthreads();
+  const unsigned who = __ballot_sync(0xffffffffu, fs >= 0);
+  if (!who) return false;
+  const int src = __ffs(who) - 1;
+  it.s = __shfl_sync(0xffffffffu, fs, src);
+  const int li = __shfl_sync(0xffffffffu, fli, src);
+  it.qs = __ldg(p.query_start_loc + it.s);
+  it.q_len = __ldg(p.query_start_loc + it.s + 1) - it.qs;
+  it.mt = (it.q_len * G + BM - 1) / BM;
+  const int npair = (it.mt + 1) / 2;
+  it.g = li % p.Hkv;
+  it.mp = npair - 1 - li / p.Hkv;  // later tiles (more keys) first
+  int ctx = __ldg(p.seq_lens + it.s);
+  const int cap = p.max_pages * kPage;
+  if (ctx > cap) ctx = cap;
+  if (ctx < it.q_len) ctx = it.q_len;  // malformed metadata; never read past the row
+  it.ctx = ctx;
+  const int m0 = 2 * it.mp, m1 = m0 + 1;
+  it.n_kv0 = (ctx - it.q_len + min(m0 * TM + TM - 1, it.q_len - 1)) / BN + 1;
+  it.n_kv1 = m1 < it.mt ? (ctx - it.q_len + min(m1 * TM + TM - 1, it.q_len - 1)) / BN + 1 : 0;
+  it.n_kv = max(it.n_kv0, it.n_kv1);
+  it.n_pages = (ctx + kPage - 1) / kPage;
+  return true;
 }
 
 template <int D, int G>
@@ -125,36 +150,12 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
   Bars *bs = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  find_tile(p, G, blockIdx.x, bs);
-  if (bs->tile_s < 0) return;  // uniform: more CTAs than work items
-  const int s = bs->tile_s;
-  const int qs = __ldg(p.query_start_loc + s);
-  const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
-  const int mt = (q_len * G + BM - 1) / BM;
-  const int npair = (mt + 1) / 2;
-  const int g = bs->tile_li % p.Hkv;
-  const int mp = npair - 1 - bs->tile_li / p.Hkv;  // later tiles (more keys) first
-  int ctx = __ldg(p.seq_lens + s);
-  const int cap = p.max_pages * kPage;
-  if (ctx > cap) ctx = cap;
-  if (ctx < q_len) return;  // malformed; the host contract forbids it
-  // the two query tiles of this CTA and the KV tiles each must visit
-  int n_kv_t[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int m = 2 * mp + i;
-    if (m < mt) {
-      const int last_tok = min(m * TM + TM - 1, q_len - 1);
-      n_kv_t[i] = (ctx - q_len + last_tok) / BN + 1;
-    } else {
-      n_kv_t[i] = 0;
-    }
-  }
-  const int n_kv = max(n_kv_t[0], n_kv_t[1]);
-  const int n_pages = (ctx + kPage - 1) / kPage;
+  const int total = warp_total_items(p, G);  // identical in every warp
+  if ((int)blockIdx.x >= total) return;      // uniform over the CTA
 
   if (tid == 0) {
-    ptx::mbar_init(&bs->q, 1);
+    ptx::mbar_init(&bs->q_full, 1);
+    ptx::mbar_init(&bs->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bs->k_full[i], 1);
       ptx::mbar_init(&bs->v_full[i], 1);
@@ -177,235 +178,272 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       ptx::prefetch_tmap(&tm_q);
       ptx::prefetch_tmap(&tm_k);
       ptx::prefetch_tmap(&tm_v);
-      const int ntiles = n_kv_t[1] > 0 ? 2 : 1;
-      ptx::mbar_arrive_expect_tx(&bs->q, ntiles * C::Q_BYTES);
-      for (int i = 0; i < ntiles; ++i)
-#pragma unroll
-        for (int pl = 0; pl < C::PANELS; ++pl)
-          ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, g * G,
-                           qs + (2 * mp + i) * TM, &bs->q);
     }
-    const int32_t *bt = p.block_table + (int64_t)s * p.max_pages;
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !ptx::mbar_wait(&bs->kv_empty[st], ((j - 2) >> 1) & 1)) {
-        if (lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
-        break;
+    uint32_t kvc = 0;  // K/V tiles loaded so far by this CTA
+    bool ok = true;
+    int n = 0;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
+      Item it;
+      if (!warp_find_item<G>(p, item, it)) break;
+      // the Q buffers are free once every MMA of the previous item completed
+      if (n > 0 && !ptx::mbar_wait(&bs->q_empty, (n - 1) & 1)) { ok = false; break; }
+      if (lane == 0) {
+        const int ntiles = it.n_kv1 > 0 ? 2 : 1;
+        ptx::mbar_arrive_expect_tx(&bs->q_full, ntiles * C::Q_BYTES);
+        for (int i = 0; i < ntiles; ++i)
+#pragma unroll
+          for (int pl = 0; pl < C::PANELS; ++pl)
+            ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, it.g * G,
+                             it.qs + (2 * it.mp + i) * TM, &bs->q_full);
       }
-      int row = kv_rows;  // out of range: zero fill
-      if (lane < 8) {
-        const int pi = j * 8 + lane;
-        if (pi < n_pages) {
-          const int page = __ldg(bt + pi);
-          if (page >= 0 && page < p.num_pages) {
-            row = (page * p.Hkv + g) * kPage;
-          } else {
-            atomicOr(p.status, STATUS_BAD_PAGE);
+      const int32_t *bt = p.block_table + (int64_t)it.s * p.max_pages;
+      for (int j = 0; j < it.n_kv; ++j, ++kvc) {
+        const int st = kvc & 1;
+        if (kvc >= 2 && !ptx::mbar_wait(&bs->kv_empty[st], ((kvc - 2) >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        int row = kv_rows;  // out of range: zero fill
+        if (lane < 8) {
+          const int pi = j * 8 + lane;
+          if (pi < it.n_pages) {
+            const int page = __ldg(bt + pi);
+            if (page >= 0 && page < p.num_pages) {
+              row = (page * p.Hkv + it.g) * kPage;
+            } else {
+              atomicOr(p.status, STATUS_BAD_PAGE);
+            }
           }
         }
-      }
-      int rows[8];
+        int rows[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, row, i);
-      if (lane == 0) {
-        unsigned char *dk = sK + st * C::KV_BYTES;
-        unsigned char *dv = sV + st * C::KV_BYTES;
-        ptx::mbar_arrive_expect_tx(&bs->k_full[st], C::KV_BYTES);
+        for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, row, i);
+        if (lane == 0) {
+          unsigned char *dk = sK + st * C::KV_BYTES;
+          unsigned char *dv = sV + st * C::KV_BYTES;
+          ptx::mbar_arrive_expect_tx(&bs->k_full[st], C::KV_BYTES);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int pl = 0; pl < C::PANELS; ++pl)
-            ptx::tma_load_2d(dk + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i],
-                             &bs->k_full[st]);
-        ptx::mbar_arrive_expect_tx(&bs->v_full[st], C::KV_BYTES);
+            for (int pl = 0; pl < C::PANELS; ++pl)
+              ptx::tma_load_2d(dk + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i],
+                               &bs->k_full[st]);
+          ptx::mbar_arrive_expect_tx(&bs->v_full[st], C::KV_BYTES);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int pl = 0; pl < C::PANELS; ++pl)
-            ptx::tma_load_2d(dv + pl * BN * 128 + i * kPage * 128, &tm_v, pl * 64, rows[i],
-                             &bs->v_full[st]);
+            for (int pl = 0; pl < C::PANELS; ++pl)
+              ptx::tma_load_2d(dv + pl * BN * 128 + i * kPage * 128, &tm_v, pl * 64, rows[i],
+                               &bs->v_full[st]);
+        }
       }
     }
+    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
     // ------------------------------- MMA issuer ---------------------------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
-      auto issue_qk = [&](int i, int j) {
-        const unsigned char *kk = sK + (j & 1) * C::KV_BYTES;
-        const unsigned char *qq = sQ + i * C::Q_BYTES;
+    constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
+    constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
+    uint32_t kvm = 0;             // K/V tiles consumed so far by this CTA
+    uint32_t pcnt[2] = {0, 0};    // P tiles consumed per query tile slot
+    bool ok = true;
+    int n = 0;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
+      Item it;
+      if (!warp_find_item<G>(p, item, it)) break;
+      if (lane == 0) {
+        auto issue_qk = [&](int i, uint32_t kvidx) {
+          const unsigned char *kk = sK + (kvidx & 1) * C::KV_BYTES;
+          const unsigned char *qq = sQ + i * C::Q_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const int pl = ks >> 2, within = (ks & 3) * 32;
-          const uint64_t a = ptx::smem_desc_sw128(qq + pl * BM * 128 + within, 16, 1024);
-          const uint64_t b = ptx::smem_desc_sw128(kk + pl * BN * 128 + within, 16, 1024);
-          ptx::mma_bf16_ss(tmem + i * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(&bs->s_full[i]);
-      };
-      bool ok = ptx::mbar_wait(&bs->q, 0) && ptx::mbar_wait(&bs->k_full[0], 0);
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_qk(0, 0);
-        if (n_kv_t[1] > 0) issue_qk(1, 0);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        bool v_ready = false, k_next_ready = false;
-        for (int i = 0; ok && i < 2; ++i) {
-          const int n_i = i ? n_kv_t[1] : n_kv_t[0];
-          if (j >= n_i) continue;
-          if (!ptx::mbar_wait(&bs->p_full[i], j & 1)) { ok = false; break; }
-          if (!v_ready) {
-            if (!ptx::mbar_wait(&bs->v_full[st], (j >> 1) & 1)) { ok = false; break; }
-            v_ready = true;
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int pl = ks >> 2, within = (ks & 3) * 32;
+            const uint64_t a = ptx::smem_desc_sw128(qq + pl * BM * 128 + within, 16, 1024);
+            const uint64_t b = ptx::smem_desc_sw128(kk + pl * BN * 128 + within, 16, 1024);
+            ptx::mma_bf16_ss(tmem + i * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
           }
+          ptx::mma_commit(&bs->s_full[i]);
+        };
+        ok = ptx::mbar_wait(&bs->q_full, n & 1) &&
+             ptx::mbar_wait(&bs->k_full[kvm & 1], (kvm >> 1) & 1);
+        if (ok) {
           ptx::tc_fence_after();
-          const unsigned char *vv = sV + st * C::KV_BYTES;
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
-            ptx::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, b, idesc_pv,
-                             (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          if (j + 1 < n_i) {
-            if (!k_next_ready) {
-              if (!ptx::mbar_wait(&bs->k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) { ok = false; break; }
-              k_next_ready = true;
-              ptx::tc_fence_after();
-            }
-            issue_qk(i, j + 1);
-          } else {
-            ptx::mma_commit(&bs->o_final[i]);
-          }
+          issue_qk(0, kvm);
+          if (it.n_kv1 > 0) issue_qk(1, kvm);
         }
-        ptx::mma_commit(&bs->kv_empty[st]);
+        for (int j = 0; ok && j < it.n_kv; ++j) {
+          const uint32_t kv = kvm + j;
+          const int st = kv & 1;
+          bool v_ready = false, k_next_ready = false;
+          for (int i = 0; ok && i < 2; ++i) {
+            const int n_i = i ? it.n_kv1 : it.n_kv0;
+            if (j >= n_i) continue;
+            uint32_t &pc = i ? pcnt[1] : pcnt[0];
+            if (!ptx::mbar_wait(&bs->p_full[i], pc & 1)) { ok = false; break; }
+            ++pc;
+            if (!v_ready) {
+              if (!ptx::mbar_wait(&bs->v_full[st], (kv >> 1) & 1)) { ok = false; break; }
+              v_ready = true;
+            }
+            ptx::tc_fence_after();
+            const unsigned char *vv = sV + st * C::KV_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
+              ptx::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, b, idesc_pv,
+                               (j > 0 || ks > 0) ? 1u : 0u);
+            }
+            if (j + 1 < n_i) {
+              if (!k_next_ready) {
+                if (!ptx::mbar_wait(&bs->k_full[(kv + 1) & 1], ((kv + 1) >> 1) & 1)) {
+                  ok = false;
+                  break;
+                }
+                k_next_ready = true;
+                ptx::tc_fence_after();
+              }
+              issue_qk(i, kv + 1);
+            } else {
+              ptx::mma_commit(&bs->o_final[i]);
+            }
+          }
+          ptx::mma_commit(&bs->kv_empty[st]);
+        }
+        ptx::mma_commit(&bs->q_empty);
       }
-      if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      kvm += it.n_kv;
     }
+    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   } else {
     // ------------------------------- softmax ------------------------------------
-    const int ti = warp >> 2;                 // query tile of this warpgroup
+    const int ti = warp >> 2;                 // query tile slot of this warpgroup
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;        // tile row
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + ti * 128 + lane_off;
     const uint32_t tO = tmem + 256 + ti * 128 + lane_off;
-    const int m = 2 * mp + ti;
-    const int n_mine = ti ? n_kv_t[1] : n_kv_t[0];
-    const int tok = m * TM + r / G;           // index within the chunk
-    const bool row_valid = tok < q_len;
-    const int last = row_valid ? ctx - q_len + tok : 0;
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = n_mine > 0;
-    for (int j = 0; ok && j < n_mine; ++j) {
-      if (!ptx::mbar_wait(&bs->s_full[ti], j & 1)) { ok = false; break; }
-      ptx::tc_fence_after();
-      // pass 1: row max over this tile's visible keys, 32 columns at a time
-      const int key0 = j * BN;
-      const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
-      const int nvis = last - key0 + 1;        // visible keys of this row in the tile
-      float mx = -INFINITY;
+    uint32_t scnt = 0, ocnt = 0, kvb = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      Item it;
+      if (!warp_find_item<G>(p, item, it)) break;
+      const int n_mine = ti ? it.n_kv1 : it.n_kv0;
+      const int ctx = it.ctx, q_len = it.q_len;
+      const int tok = (2 * it.mp + ti) * TM + r / G;  // index within the chunk
+      const bool row_valid = tok < q_len;
+      const int last = row_valid ? ctx - q_len + tok : 0;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n_mine; ++j, ++scnt) {
+        if (!ptx::mbar_wait(&bs->s_full[ti], scnt & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        // pass 1: row max over this tile's visible keys, 32 columns at a time
+        const int key0 = j * BN;
+        const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
+        const int nvis = last - key0 + 1;        // visible keys of this row in the tile
+        float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        ptx::tmem_ld32(tS + c * 32, sr);
-        ptx::tmem_wait_ld();
-        if (diag) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          ptx::tmem_ld32(tS + c * 32, sr);
+          ptx::tmem_wait_ld();
+          if (diag) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx = ptx::max3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-      }
-      const float mnew = fmaxf(m_run, mx * sl2);
-      if (j == 0) {
-        m_run = mnew;
-      } else {
-        // Rescale O only when a row's running max grew by more than the
-        // threshold.  TMEM loads/stores are warp-collective, so the whole warp
-        // takes the branch if any of its rows needs it (the others scale by 1).
-        // S_j being complete implies PV_{j-1} has completed (same issuing
-        // thread, in order), so O is current.
-        const bool need = mnew > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ptx::ex2(m_run - mnew) : 1.f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + c * 32, o);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st32(tO + c * 32, o);
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
           }
-          if (need) {
-            l_run *= alpha;
-            m_run = mnew;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            mx = ptx::max3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+        }
+        const float mnew = fmaxf(m_run, mx * sl2);
+        if (j == 0) {
+          m_run = mnew;
+        } else {
+          // Rescale O only when a row's running max grew by more than the
+          // threshold.  TMEM loads/stores are warp-collective, so the whole
+          // warp takes the branch if any of its rows needs it (the others
+          // scale by 1).  S_j being complete implies PV_{j-1} has completed
+          // (same issuing thread, in order), so O is current.
+          const bool need = mnew > m_run + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ptx::ex2(m_run - mnew) : 1.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + c * 32, o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              ptx::tmem_st32(tO + c * 32, o);
+            }
+            if (need) {
+              l_run *= alpha;
+              m_run = mnew;
+            }
           }
         }
-      }
-      // pass 2: P = exp2(S * scale - m) in bf16, written over S.  P chunk c
-      // (columns [16c, 16c + 16)) only overwrites S columns already consumed.
-      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-      const uint64_t sc2 = ptx::pack2(sl2, sl2);
-      const uint64_t nm2 = ptx::pack2(-mref, -mref);
-      uint64_t rs2 = 0ull;
+        // pass 2: P = exp2(S * scale - m) in bf16, written over S.  P chunk c
+        // (columns [16c, 16c + 16)) only overwrites S columns already consumed.
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+        const uint64_t sc2 = ptx::pack2(sl2, sl2);
+        const uint64_t nm2 = ptx::pack2(-mref, -mref);
+        uint64_t rs2 = 0ull;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], pw[16];
-        ptx::tmem_ld32(tS + c * 32, sr);
-        ptx::tmem_wait_ld();
-        if (diag) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32], pw[16];
+          ptx::tmem_ld32(tS + c * 32, sr);
+          ptx::tmem_wait_ld();
+          if (diag) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 32; ++e)
+              if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const uint64_t x2 = ptx::ffma2(
+                ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
+            float x0, x1;
+            ptx::unpack2(x2, x0, x1);
+            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+            rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
+            pw[h] = ptx::pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st16(tS + c * 16, pw);
         }
+        float rs0, rs1;
+        ptx::unpack2(rs2, rs0, rs1);
+        l_run += rs0 + rs1;
+        // Cache slots at or past ctx in the last page may hold anything (NaN
+        // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
+        // runs.  Both warpgroups may write the same zeros; rows past the last
+        // page were loaded out of range and are zero already.
+        if (key0 + BN > ctx) {
+          const uint32_t kv = kvb + j;
+          if (!ptx::mbar_wait(&bs->v_full[kv & 1], (kv >> 1) & 1)) { ok = false; break; }
+          if (r >= ctx - key0 && r < it.n_pages * kPage - key0) {
+            unsigned char *vrow = sV + (kv & 1) * C::KV_BYTES + r * 128;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const uint64_t x2 = ptx::ffma2(
-              ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
-          float x0, x1;
-          ptx::unpack2(x2, x0, x1);
-          const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-          rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
-          pw[h] = ptx::pack_bf16x2(p0, p1);
+            for (int pl = 0; pl < C::PANELS; ++pl)
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(vrow + pl * BN * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          ptx::fence_proxy_async_smem();
         }
-        ptx::tmem_st16(tS + c * 16, pw);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&bs->p_full[ti]);
       }
-      float rs0, rs1;
-      ptx::unpack2(rs2, rs0, rs1);
-      l_run += rs0 + rs1;
-      // Cache slots at or past ctx in the last page may hold anything (NaN
-      // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
-      // runs.  Both warpgroups may write the same zeros; rows past the last
-      // page were loaded out of range and are zero already.
-      if (key0 + BN > ctx) {
-        const int st = j & 1;
-        if (!ptx::mbar_wait(&bs->v_full[st], (j >> 1) & 1)) { ok = false; break; }
-        if (r >= ctx - key0 && r < n_pages * kPage - key0) {
-          unsigned char *vrow = sV + st * C::KV_BYTES + r * 128;
-#pragma unroll
-          for (int pl = 0; pl < C::PANELS; ++pl)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4 *>(vrow + pl * BN * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-        ptx::fence_proxy_async_smem();
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&bs->p_full[ti]);
-    }
-    // epilogue: O / l
-    if (ok && ptx::mbar_wait(&bs->o_final[ti], 0)) {
+      kvb += it.n_kv;
+      if (!ok || n_mine == 0) continue;
+      // epilogue: O / l
+      if (!ptx::mbar_wait(&bs->o_final[ti], ocnt & 1)) { ok = false; break; }
+      ++ocnt;
       ptx::tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
-                           ((int64_t)(qs + tok) * p.Hq + g * G + r % G) * D;
+                           ((int64_t)(it.qs + tok) * p.Hq + it.g * G + r % G) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -424,9 +462,10 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           }
         }
       }
-    } else if (n_mine > 0) {
-      atomicOr(p.status, STATUS_TIMEOUT);
+      // O is read; the next item's first PV may overwrite it after p_full
+      ptx::tc_fence_before();
     }
+    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   }
 
   ptx::tc_fence_before();
@@ -452,7 +491,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int D, int G>
-cudaError_t launch_dg(const AttnParams &p, cudaStream_t stream) {
+cudaError_t launch_dg(const AttnParams &p, int grid, cudaStream_t stream) {
   using C = ChunkCfg<D>;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -489,12 +528,7 @@ cudaError_t launch_dg(const AttnParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  // upper bound on work items (pairs of 128-row tiles): every chunk adds at
-  // most one partial pair per kv head
-  const int64_t grid =
-      (int64_t)p.Hkv * (((int64_t)p.num_tokens * G + 2 * BM - 1) / (2 * BM) + p.num_seqs);
-  attn_chunk_kernel<D, G><<<(unsigned)grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv,
-                                                                        (int)rows);
+  attn_chunk_kernel<D, G><<<grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv, (int)rows);
   return cudaGetLastError();
 }
 
@@ -506,21 +540,32 @@ bool chunk_tc_path(int dtype, int D, int G) {
   return G == 1 || G == 2 || G == 4 || G == 8;
 }
 
-cudaError_t launch_attention_chunk(const AttnParams &p, cudaStream_t stream) {
+int chunk_grid_estimate(const AttnParams &p, int sms) {
+  // Persistent grid: one CTA per expected work item (pairs of 128-row tiles),
+  // assuming the step's chunk tokens are num_tokens - num_seqs + 1 (one chunk
+  // among decodes); any count is correct, this only sets the SM split.
+  const int G = p.Hq / p.Hkv;
+  const int64_t chunk_tokens = (int64_t)p.num_tokens - p.num_seqs + 1;
+  const int64_t pairs = (chunk_tokens * G + 2 * BM - 1) / (2 * BM);
+  const int64_t est = (int64_t)p.Hkv * pairs;
+  return (int)(est < 1 ? 1 : (est > sms ? sms : est));
+}
+
+cudaError_t launch_attention_chunk(const AttnParams &p, int grid, cudaStream_t stream) {
   const int G = p.Hq / p.Hkv;
   if (p.D == 128) {
     switch (G) {
-      case 1: return launch_dg<128, 1>(p, stream);
-      case 2: return launch_dg<128, 2>(p, stream);
-      case 4: return launch_dg<128, 4>(p, stream);
-      case 8: return launch_dg<128, 8>(p, stream);
+      case 1: return launch_dg<128, 1>(p, grid, stream);
+      case 2: return launch_dg<128, 2>(p, grid, stream);
+      case 4: return launch_dg<128, 4>(p, grid, stream);
+      case 8: return launch_dg<128, 8>(p, grid, stream);
     }
   } else {
     switch (G) {
-      case 1: return launch_dg<64, 1>(p, stream);
-      case 2: return launch_dg<64, 2>(p, stream);
-      case 4: return launch_dg<64, 4>(p, stream);
-      case 8: return launch_dg<64, 8>(p, stream);
+      case 1: return launch_dg<64, 1>(p, grid, stream);
+      case 2: return launch_dg<64, 2>(p, grid, stream);
+      case 4: return launch_dg<64, 4>(p, grid, stream);
+      case 8: return launch_dg<64, 8>(p, grid, stream);
     }
   }
   return cudaErrorInvalidValue;

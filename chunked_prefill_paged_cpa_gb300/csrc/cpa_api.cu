@@ -1,6 +1,6 @@
 // C ABI of libcpa: argument validation, workspace layout and launches.
 // Declared and documented in include/cpa.h.
-#include <stdio.h>
+#include <mutex>
 
 #include "cpa_internal.cuh"
 
@@ -44,6 +44,32 @@ int decode_grid(int device) {
     sms[device] = n;
   }
   return sms[device];
+}
+
+// Per-device side stream and fork/join events used to run the chunk tiles
+// (tensor-bound) beside the decode stream (HBM-bound).  Created on first use;
+// they are CUDA objects, not device memory.  A mutex keeps the record/wait
+// sequence of concurrent host threads from interleaving.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static SideStream g_side[64];
+static std::mutex g_side_mutex;
+
+static SideStream *side_stream(int device) {
+  if (device < 0 || device >= 64) return nullptr;
+  SideStream &ss = g_side[device];
+  if (!ss.stream) {
+    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      ss.stream = nullptr;
+      return nullptr;
+    }
+  }
+  return &ss;
 }
 
 // Shape checks shared by both calls.
@@ -158,20 +184,52 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
   if (tc_chunks && (int64_t)p.num_pages * p.Hkv * p.page_size >= INT32_MAX)
     return CPA_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
   bool rows_for_decodes = true, rows_for_chunks = !all_decode;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
+  const int sms = decode_grid(dev);
+  if (sms <= 0) return CPA_ERR_CUDA;
   if (w.fast_decode) {
     if (num_seqs > kDecodeMaxSeqs) return CPA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
-    int grid = decode_grid(dev);
-    if (grid <= 0) return CPA_ERR_CUDA;
-    if (grid * 8 > kDecodeMaxWorkers) grid = kDecodeMaxWorkers / 8;
-    if (launch_attention_decode(p, grid, st) != cudaSuccess) return CPA_ERR_CUDA;
-    rows_for_decodes = false;
   }
-  if (tc_chunks && !all_decode) {
-    if (launch_attention_chunk(p, st) != cudaSuccess) return CPA_ERR_CUDA;
-    rows_for_chunks = false;
+  const bool launch_chunks = tc_chunks && !all_decode;
+  if (launch_chunks && w.fast_decode) {
+    // Both kernels hold one CTA per SM.  When the chunk tiles leave enough
+    // SMs free, run them on the side stream while the decodes stream on the
+    // caller's stream over the remaining SMs; otherwise run them one after
+    // the other on the caller's stream.
+    const int cg = chunk_grid_estimate(p, sms);
+    int dg = sms - cg;
+    if (dg > kDecodeMaxWorkers / 8) dg = kDecodeMaxWorkers / 8;
+    if (dg >= sms / 8) {
+      std::lock_guard<std::mutex> lock(g_side_mutex);
+      SideStream *ss = side_stream(dev);
+      if (!ss) return CPA_ERR_CUDA;
+      if (cudaEventRecord(ss->fork, st) != cudaSuccess ||
+          cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+        return CPA_ERR_CUDA;
+      if (launch_attention_chunk(p, cg, ss->stream) != cudaSuccess) return CPA_ERR_CUDA;
+      if (launch_attention_decode(p, dg, st) != cudaSuccess) return CPA_ERR_CUDA;
+      if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
+          cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
+        return CPA_ERR_CUDA;
+    } else {
+      if (launch_attention_chunk(p, cg, st) != cudaSuccess) return CPA_ERR_CUDA;
+      int g2 = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
+      if (launch_attention_decode(p, g2, st) != cudaSuccess) return CPA_ERR_CUDA;
+    }
+    rows_for_decodes = rows_for_chunks = false;
+  } else {
+    if (w.fast_decode) {
+      int g2 = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
+      if (launch_attention_decode(p, g2, st) != cudaSuccess) return CPA_ERR_CUDA;
+      rows_for_decodes = false;
+    }
+    if (launch_chunks) {
+      if (launch_attention_chunk(p, chunk_grid_estimate(p, sms), st) != cudaSuccess)
+        return CPA_ERR_CUDA;
+      rows_for_chunks = false;
+    }
   }
   if (!rows_for_decodes && !rows_for_chunks) return CPA_OK;
   p.rows_mode = (rows_for_decodes && rows_for_chunks) ? 0 : (rows_for_chunks ? 1 : 2);

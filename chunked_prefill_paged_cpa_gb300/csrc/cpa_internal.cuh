@@ -76,7 +76,8 @@ int decode_grid(int device);
 
 // Prefill-chunk tiles on tcgen05 (bf16; head_dim 64/128; GQA group 1/2/4/8).
 bool chunk_tc_path(int dtype, int D, int G);
-cudaError_t launch_attention_chunk(const AttnParams &p, cudaStream_t stream);
+cudaError_t launch_attention_chunk(const AttnParams &p, int grid, cudaStream_t stream);
+int chunk_grid_estimate(const AttnParams &p, int sms);
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

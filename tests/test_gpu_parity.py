@@ -169,6 +169,37 @@ def test_decode_batches(cuda_device, case):
     assert torch.equal(bits(out), bits(out2))
 
 
+MULTI_CHUNK_CASES = [
+    # (decode contexts, [(chunk q_len, cached prefix)]) -- Llama-3-8B shape, bf16
+    ([600, 33, 1500, 17] * 10, [(100, 37), (100, 500)]),      # concurrent kernels
+    ([2000, 90, 4100, 700, 1], [(1000, 0), (1000, 333), (1000, 2000)]),  # items > CTAs
+    ([], [(64, 0), (65, 15), (129, 16), (2, 5000)]),          # chunks only, tiny tiles
+    ([5000] * 3, [(257, 4096)]),                             # page-aligned prefix, ragged tile
+]
+
+
+@pytest.mark.parametrize("case", range(len(MULTI_CHUNK_CASES)))
+def test_multiple_chunks_per_step(cuda_device, case):
+    """Several prefill chunks (with cached prefixes that need not be
+    page-aligned) beside decodes in one step."""
+    dec, chunks = MULTI_CHUNK_CASES[case]
+    q_lens = [1] * len(dec) + [c for c, _ in chunks]
+    seq_lens = list(dec) + [c + pre for c, pre in chunks]
+    st = make_step(q_lens, seq_lens, 32, 8, 128, torch.bfloat16, seed=900 + case)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(128)
+    out, wsp = gpu_step(k_cache, v_cache, inp, scale, 32)
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    assert_close(out.cpu(), want, f"multi-chunk case {case}")
+    assert ops.device_status(k_cache, 32, m.block_table.shape[1], wsp) == 0
+
+
 def test_ones_values_give_ones_and_onehot_values_give_probabilities(cuda_device):
     """V == 1 makes every output 1 (softmax rows sum to 1, including across
     merged splits); V_j = e_j (ctx <= D) makes the output row the probability
