@@ -49,15 +49,17 @@ struct ChunkCfg {
   static constexpr int PANELS = D / 64;          // 128-byte swizzle panels along head_dim
   static constexpr int Q_BYTES = BM * D * 2;     // one query tile
   static constexpr int KV_BYTES = BN * D * 2;    // one K (or V) tile
+  static constexpr int KST = 3, VST = 2;       // K and V ring depths
   static constexpr int OFF_Q = 0;                // two query tiles
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers, scan scratch, 1 KB alignment
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, k_full[2], v_full[2], kv_empty[2], s_full[2], p_full[2], o_final[2];
+  uint64_t q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
+      o_final[2];
   uint32_t tmem_base;
 };
 
@@ -134,6 +136,31 @@ __device__ bool warp_find_item(const AttnParams &p, int item, Item &it) {
   return true;
 }
 
+// Keys at positions >= n of a 32-column chunk become -inf.
+__device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (e >= n) sr[e] = __float_as_uint(-INFINITY);
+}
+
+// p = exp2(s * scale - m) for 32 columns: bf16 pairs to TMEM (16 columns at
+// `dst`), fp32 row sum accumulated in `rs2` (packed pair).
+__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
+                                          uint64_t &rs2, uint32_t dst) {
+  uint32_t pw[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+    const uint64_t x2 = ptx::ffma2(
+        ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
+    float x0, x1;
+    ptx::unpack2(x2, x0, x1);
+    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+    rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
+    pw[h] = ptx::pack_bf16x2(p0, p1);
+  }
+  ptx::tmem_st16(dst, pw);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -156,10 +183,13 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
   if (tid == 0) {
     ptx::mbar_init(&bs->q_full, 1);
     ptx::mbar_init(&bs->q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&bs->k_full[i], 1);
+      ptx::mbar_init(&bs->k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bs->v_full[i], 1);
-      ptx::mbar_init(&bs->kv_empty[i], 1);
+      ptx::mbar_init(&bs->v_empty[i], 1);
       ptx::mbar_init(&bs->s_full[i], 1);
       ptx::mbar_init(&bs->p_full[i], 128);
       ptx::mbar_init(&bs->o_final[i], 1);
@@ -196,47 +226,62 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, it.g * G,
                              it.qs + (2 * it.mp + i) * TM, &bs->q_full);
       }
+      // page ids of the item, 32 at a time in this warp's registers (lane l
+      // holds page 32 b + l of block b), the next block prefetched
       const int32_t *bt = p.block_table + (int64_t)it.s * p.max_pages;
-      for (int j = 0; j < it.n_kv; ++j, ++kvc) {
-        const int st = kvc & 1;
-        if (kvc >= 2 && !ptx::mbar_wait(&bs->kv_empty[st], ((kvc - 2) >> 1) & 1)) {
-          ok = false;
-          break;
+      auto load_block = [&](int b) -> int {
+        const int pi = 32 * b + lane;
+        if (pi >= it.n_pages) return kv_rows;  // past the sequence: zero fill
+        const int page = __ldg(bt + pi);
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.status, STATUS_BAD_PAGE);
+          return kv_rows;
         }
-        int row = kv_rows;  // out of range: zero fill
-        if (lane < 8) {
-          const int pi = j * 8 + lane;
-          if (pi < it.n_pages) {
-            const int page = __ldg(bt + pi);
-            if (page >= 0 && page < p.num_pages) {
-              row = (page * p.Hkv + it.g) * kPage;
-            } else {
-              atomicOr(p.status, STATUS_BAD_PAGE);
-            }
-          }
+        return (page * p.Hkv + it.g) * kPage;
+      };
+      // V lags K by one tile, so the block before the current one is kept too
+      int blk_prev = kv_rows, blk_cur = load_block(0), blk_next = load_block(1), blk = 0;
+      auto load_tile = [&](unsigned char *dst, const CUtensorMap *tm, uint64_t *bar, int j) {
+        const int b = j >> 2;
+        while (blk < b) {  // warp-uniform
+          blk_prev = blk_cur;
+          blk_cur = blk_next;
+          ++blk;
+          blk_next = load_block(blk + 1);
         }
+        const int src = (b == blk) ? blk_cur : blk_prev;  // b is blk or blk - 1
         int rows[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, row, i);
+        for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, src, (j & 3) * 8 + i);
         if (lane == 0) {
-          unsigned char *dk = sK + st * C::KV_BYTES;
-          unsigned char *dv = sV + st * C::KV_BYTES;
-          ptx::mbar_arrive_expect_tx(&bs->k_full[st], C::KV_BYTES);
+          ptx::mbar_arrive_expect_tx(bar, C::KV_BYTES);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int pl = 0; pl < C::PANELS; ++pl)
-              ptx::tma_load_2d(dk + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i],
-                               &bs->k_full[st]);
-          ptx::mbar_arrive_expect_tx(&bs->v_full[st], C::KV_BYTES);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int pl = 0; pl < C::PANELS; ++pl)
-              ptx::tma_load_2d(dv + pl * BN * 128 + i * kPage * 128, &tm_v, pl * 64, rows[i],
-                               &bs->v_full[st]);
+              ptx::tma_load_2d(dst + pl * BN * 128 + i * kPage * 128, tm, pl * 64, rows[i], bar);
+        }
+      };
+      // K runs one tile ahead of V: K_t, then V_{t-1}
+      for (int t = 0; t <= it.n_kv; ++t) {
+        if (t < it.n_kv) {
+          const uint32_t kc = kvc + t, st = kc % C::KST;
+          if (kc >= C::KST && !ptx::mbar_wait(&bs->k_empty[st], ((kc / C::KST) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          load_tile(sK + st * C::KV_BYTES, &tm_k, &bs->k_full[st], t);
+        }
+        if (t >= 1) {
+          const uint32_t vc = kvc + t - 1, st = vc % C::VST;
+          if (vc >= C::VST && !ptx::mbar_wait(&bs->v_empty[st], ((vc / C::VST) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          load_tile(sV + st * C::KV_BYTES, &tm_v, &bs->v_full[st], t - 1);
         }
       }
+      kvc += it.n_kv;
     }
     if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   } else if (warp == kMmaWarp) {
@@ -244,7 +289,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
     constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
     uint32_t kvm = 0;             // K/V tiles consumed so far by this CTA
-    uint32_t pcnt[2] = {0, 0};    // P tiles consumed per query tile slot
+    uint32_t pcnt0 = 0, pcnt1 = 0;  // P tiles consumed per query tile slot
     bool ok = true;
     int n = 0;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
@@ -252,7 +297,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       if (!warp_find_item<G>(p, item, it)) break;
       if (lane == 0) {
         auto issue_qk = [&](int i, uint32_t kvidx) {
-          const unsigned char *kk = sK + (kvidx & 1) * C::KV_BYTES;
+          const unsigned char *kk = sK + (kvidx % C::KST) * C::KV_BYTES;
           const unsigned char *qq = sQ + i * C::Q_BYTES;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
@@ -264,28 +309,29 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           ptx::mma_commit(&bs->s_full[i]);
         };
         ok = ptx::mbar_wait(&bs->q_full, n & 1) &&
-             ptx::mbar_wait(&bs->k_full[kvm & 1], (kvm >> 1) & 1);
+             ptx::mbar_wait(&bs->k_full[kvm % C::KST], (kvm / C::KST) & 1);
         if (ok) {
           ptx::tc_fence_after();
           issue_qk(0, kvm);
           if (it.n_kv1 > 0) issue_qk(1, kvm);
+          ptx::mma_commit(&bs->k_empty[kvm % C::KST]);
         }
         for (int j = 0; ok && j < it.n_kv; ++j) {
           const uint32_t kv = kvm + j;
-          const int st = kv & 1;
+          const int vst = kv % C::VST;
           bool v_ready = false, k_next_ready = false;
           for (int i = 0; ok && i < 2; ++i) {
             const int n_i = i ? it.n_kv1 : it.n_kv0;
             if (j >= n_i) continue;
-            uint32_t &pc = i ? pcnt[1] : pcnt[0];
+            const uint32_t pc = i ? pcnt1 : pcnt0;
             if (!ptx::mbar_wait(&bs->p_full[i], pc & 1)) { ok = false; break; }
-            ++pc;
+            if (i) ++pcnt1; else ++pcnt0;
             if (!v_ready) {
-              if (!ptx::mbar_wait(&bs->v_full[st], (kv >> 1) & 1)) { ok = false; break; }
+              if (!ptx::mbar_wait(&bs->v_full[vst], (kv / C::VST) & 1)) { ok = false; break; }
               v_ready = true;
             }
             ptx::tc_fence_after();
-            const unsigned char *vv = sV + st * C::KV_BYTES;
+            const unsigned char *vv = sV + vst * C::KV_BYTES;
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
               const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
@@ -294,7 +340,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             }
             if (j + 1 < n_i) {
               if (!k_next_ready) {
-                if (!ptx::mbar_wait(&bs->k_full[(kv + 1) & 1], ((kv + 1) >> 1) & 1)) {
+                if (!ptx::mbar_wait(&bs->k_full[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) {
                   ok = false;
                   break;
                 }
@@ -306,7 +352,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
               ptx::mma_commit(&bs->o_final[i]);
             }
           }
-          ptx::mma_commit(&bs->kv_empty[st]);
+          // V_j has no later reader; K_{j+1} was last read by this iteration's QKs
+          ptx::mma_commit(&bs->v_empty[vst]);
+          if (k_next_ready) ptx::mma_commit(&bs->k_empty[(kv + 1) % C::KST]);
         }
         ptx::mma_commit(&bs->q_empty);
       }
@@ -337,24 +385,26 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       for (int j = 0; j < n_mine; ++j, ++scnt) {
         if (!ptx::mbar_wait(&bs->s_full[ti], scnt & 1)) { ok = false; break; }
         ptx::tc_fence_after();
-        // pass 1: row max over this tile's visible keys, 32 columns at a time
+        // pass 1: row max over this tile's visible keys (two loads per wait)
         const int key0 = j * BN;
         const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
         const int nvis = last - key0 + 1;        // visible keys of this row in the tile
         float mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          ptx::tmem_ld32(tS + c * 32, sr);
+        for (int c2 = 0; c2 < 4; c2 += 2) {
+          uint32_t sa[32], sb[32];
+          ptx::tmem_ld32(tS + c2 * 32, sa);
+          ptx::tmem_ld32(tS + c2 * 32 + 32, sb);
           ptx::tmem_wait_ld();
           if (diag) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
+            mask_chunk(sa, nvis - c2 * 32);
+            mask_chunk(sb, nvis - c2 * 32 - 32);
           }
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mx = ptx::max3(mx, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+          for (int e = 0; e < 32; e += 2) {
+            mx = ptx::max3(mx, __uint_as_float(sa[e]), __uint_as_float(sa[e + 1]));
+            mx = ptx::max3(mx, __uint_as_float(sb[e]), __uint_as_float(sb[e + 1]));
+          }
         }
         const float mnew = fmaxf(m_run, mx * sl2);
         if (j == 0) {
@@ -368,7 +418,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           const bool need = mnew > m_run + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
             const float alpha = need ? ptx::ex2(m_run - mnew) : 1.f;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
               ptx::tmem_ld32(tO + c * 32, o);
@@ -384,32 +434,27 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           }
         }
         // pass 2: P = exp2(S * scale - m) in bf16, written over S.  P chunk c
-        // (columns [16c, 16c + 16)) only overwrites S columns already consumed.
+        // (columns [16c, 16c + 16)) only overwrites S columns already consumed;
+        // the load of chunk c + 1 is in flight while chunk c is converted.
         const float mref = (m_run == -INFINITY) ? 0.f : m_run;
         const uint64_t sc2 = ptx::pack2(sl2, sl2);
         const uint64_t nm2 = ptx::pack2(-mref, -mref);
         uint64_t rs2 = 0ull;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32], pw[16];
-          ptx::tmem_ld32(tS + c * 32, sr);
+        {
+          uint32_t sa[32], sb[32];
+          ptx::tmem_ld32(tS, sa);
           ptx::tmem_wait_ld();
-          if (diag) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e >= nvis) sr[e] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 4; c += 2) {
+            ptx::tmem_ld32(tS + (c + 1) * 32, sb);
+            if (diag) mask_chunk(sa, nvis - c * 32);
+            exp_chunk(sa, sc2, nm2, rs2, tS + c * 16);
+            ptx::tmem_wait_ld();
+            if (c + 2 < 4) ptx::tmem_ld32(tS + (c + 2) * 32, sa);
+            if (diag) mask_chunk(sb, nvis - (c + 1) * 32);
+            exp_chunk(sb, sc2, nm2, rs2, tS + (c + 1) * 16);
+            if (c + 2 < 4) ptx::tmem_wait_ld();
           }
-#pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const uint64_t x2 = ptx::ffma2(
-                ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
-            float x0, x1;
-            ptx::unpack2(x2, x0, x1);
-            const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-            rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
-            pw[h] = ptx::pack_bf16x2(p0, p1);
-          }
-          ptx::tmem_st16(tS + c * 16, pw);
         }
         float rs0, rs1;
         ptx::unpack2(rs2, rs0, rs1);
@@ -420,9 +465,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         // page were loaded out of range and are zero already.
         if (key0 + BN > ctx) {
           const uint32_t kv = kvb + j;
-          if (!ptx::mbar_wait(&bs->v_full[kv & 1], (kv >> 1) & 1)) { ok = false; break; }
+          if (!ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1)) { ok = false; break; }
           if (r >= ctx - key0 && r < it.n_pages * kPage - key0) {
-            unsigned char *vrow = sV + (kv & 1) * C::KV_BYTES + r * 128;
+            unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + r * 128;
 #pragma unroll
             for (int pl = 0; pl < C::PANELS; ++pl)
 #pragma unroll

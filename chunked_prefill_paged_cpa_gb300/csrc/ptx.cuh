@@ -73,6 +73,22 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- per-thread asynchronous copies (cp.async) --------------------------------
+
+// 16-byte global -> shared copy; bytes past `src_bytes` (0 or 16) are zero-filled.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem,
+                                           uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               ::"r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // ---- tensor-map (tiled) bulk copies -----------------------------------------
 
 __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, int c0, int c1,
