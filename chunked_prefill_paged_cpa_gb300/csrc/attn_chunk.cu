@@ -14,15 +14,18 @@
 //
 // Per CTA (320 threads, one CTA per SM):
 //   warps 0-3  softmax for tile 0, warps 4-7 softmax for tile 1; one thread
-//              per row.  Load S from TMEM, causal mask (diagonal tiles only),
-//              running max in the log2 domain with lazy rescaling of the TMEM
-//              O accumulator (only when the max grows by more than 2^8), exp2,
-//              row sum, and P in bf16 written back into TMEM over S.
+//              per row.  One pass over S in TMEM: causal mask (diagonal
+//              tiles only), exp2 against the running max of the earlier tiles
+//              (log2 domain) while the tile's own max is tracked, row sum, and
+//              P in bf16 written back into TMEM over S.  The running max (and
+//              with it the TMEM O accumulator) moves only when it grew by more
+//              than 2^8; the first tile and a jump past 2^64 are redone.
 //   warp 8     TMA producer: both Q tiles (3-d tensor map over q, 128-byte
 //              swizzle), then per KV tile of BN = 128 keys the 8 pages of K
 //              and of V of kv head g (2-d tensor map over the cache rows);
 //              pages past the sequence are read from an out-of-range row and
-//              arrive as zeros.  Two K/V stages.
+//              arrive as zeros.  K ring of 3 stages, V ring of 2; K runs
+//              one tile ahead of V.
 //   warp 9     allocates the 512 TMEM columns (S0, S1, O0, O1); lane 0 issues
 //              every tcgen05.mma: S_i = Q_i K_j^T (both operands from shared
 //              memory) and O_i += P_i V_j (P from TMEM, V MN-major in shared
@@ -43,6 +46,7 @@ constexpr int BN = 128;          // keys per KV tile (8 pages)
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLazyMax = 64.0f;          // log2 units: largest tolerated P exponent
 
 template <int D>
 struct ChunkCfg {
@@ -143,22 +147,21 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
     if (e >= n) sr[e] = __float_as_uint(-INFINITY);
 }
 
-// p = exp2(s * scale - m) for 32 columns: bf16 pairs to TMEM (16 columns at
-// `dst`), fp32 row sum accumulated in `rs2` (packed pair).
-__device__ __forceinline__ void exp_chunk(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
-                                          uint64_t &rs2, uint32_t dst) {
-  uint32_t pw[16];
+// p = exp2(s * scale - m) for 32 columns, kept as bf16 pairs in `pw` (16
+// words); fp32 row sum accumulated in `rs2` (packed pair); raw max of s in mx.
+__device__ __forceinline__ void exp_chunk_regs(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
+                                               uint64_t &rs2, float &mx, uint32_t *pw) {
 #pragma unroll
   for (int h = 0; h < 16; ++h) {
-    const uint64_t x2 = ptx::ffma2(
-        ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])), sc2, nm2);
+    const float s0 = __uint_as_float(sr[2 * h]), s1 = __uint_as_float(sr[2 * h + 1]);
+    mx = ptx::max3(mx, s0, s1);
+    const uint64_t x2 = ptx::ffma2(ptx::pack2(s0, s1), sc2, nm2);
     float x0, x1;
     ptx::unpack2(x2, x0, x1);
     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
     rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
     pw[h] = ptx::pack_bf16x2(p0, p1);
   }
-  ptx::tmem_st16(dst, pw);
 }
 
 template <int D, int G>
@@ -381,84 +384,108 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       const int tok = (2 * it.mp + ti) * TM + r / G;  // index within the chunk
       const bool row_valid = tok < q_len;
       const int last = row_valid ? ctx - q_len + tok : 0;
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = -INFINITY, l_run = 0.f, alpha_pending = 1.f;
+      bool rescale_pending = false;
       for (int j = 0; j < n_mine; ++j, ++scnt) {
         if (!ptx::mbar_wait(&bs->s_full[ti], scnt & 1)) { ok = false; break; }
         ptx::tc_fence_after();
-        // pass 1: row max over this tile's visible keys (two loads per wait)
         const int key0 = j * BN;
         const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
         const int nvis = last - key0 + 1;        // visible keys of this row in the tile
+        // One pass over S (4 chunks of 32 columns, the next chunk's TMEM load in
+        // flight): p = exp2(S * scale - m_run) against the running max of the
+        // earlier tiles, kept in registers as bf16 pairs while this tile's own
+        // max is tracked.  P and the row sum stay finite as long as the tile
+        // max exceeds m_run by less than 2^kLazyMax (bf16 and fp32 both reach
+        // 2^127), so the running max is only moved -- O and l rescaled -- when
+        // it grew by more than 2^8; a tile whose max jumps by more than
+        // 2^kLazyMax, and the first tile, are redone against their true max.
+        uint32_t pw[BN / 2];
         float mx = -INFINITY;
-#pragma unroll
-        for (int c2 = 0; c2 < 4; c2 += 2) {
-          uint32_t sa[32], sb[32];
-          ptx::tmem_ld32(tS + c2 * 32, sa);
-          ptx::tmem_ld32(tS + c2 * 32 + 32, sb);
-          ptx::tmem_wait_ld();
-          if (diag) {
-            mask_chunk(sa, nvis - c2 * 32);
-            mask_chunk(sb, nvis - c2 * 32 - 32);
-          }
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            mx = ptx::max3(mx, __uint_as_float(sa[e]), __uint_as_float(sa[e + 1]));
-            mx = ptx::max3(mx, __uint_as_float(sb[e]), __uint_as_float(sb[e + 1]));
-          }
-        }
-        const float mnew = fmaxf(m_run, mx * sl2);
-        if (j == 0) {
-          m_run = mnew;
-        } else {
-          // Rescale O only when a row's running max grew by more than the
-          // threshold.  TMEM loads/stores are warp-collective, so the whole
-          // warp takes the branch if any of its rows needs it (the others
-          // scale by 1).  S_j being complete implies PV_{j-1} has completed
-          // (same issuing thread, in order), so O is current.
-          const bool need = mnew > m_run + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ptx::ex2(m_run - mnew) : 1.f;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              ptx::tmem_ld32(tO + c * 32, o);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              ptx::tmem_st32(tO + c * 32, o);
-            }
-            if (need) {
-              l_run *= alpha;
-              m_run = mnew;
-            }
-          }
-        }
-        // pass 2: P = exp2(S * scale - m) in bf16, written over S.  P chunk c
-        // (columns [16c, 16c + 16)) only overwrites S columns already consumed;
-        // the load of chunk c + 1 is in flight while chunk c is converted.
-        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-        const uint64_t sc2 = ptx::pack2(sl2, sl2);
-        const uint64_t nm2 = ptx::pack2(-mref, -mref);
+        const float mref0 = (j == 0) ? INFINITY : m_run;  // first tile: no reference yet
         uint64_t rs2 = 0ull;
         {
+          const uint64_t sc2 = ptx::pack2(sl2, sl2);
+          const uint64_t nm2 = ptx::pack2(-mref0, -mref0);
           uint32_t sa[32], sb[32];
           ptx::tmem_ld32(tS, sa);
-          ptx::tmem_wait_ld();
+          ptx::tmem_wait_ld_regs(sa);
 #pragma unroll
           for (int c = 0; c < 4; c += 2) {
             ptx::tmem_ld32(tS + (c + 1) * 32, sb);
             if (diag) mask_chunk(sa, nvis - c * 32);
-            exp_chunk(sa, sc2, nm2, rs2, tS + c * 16);
-            ptx::tmem_wait_ld();
+            exp_chunk_regs(sa, sc2, nm2, rs2, mx, pw + c * 16);
+            ptx::tmem_wait_ld_regs(sb);
             if (c + 2 < 4) ptx::tmem_ld32(tS + (c + 2) * 32, sa);
             if (diag) mask_chunk(sb, nvis - (c + 1) * 32);
-            exp_chunk(sb, sc2, nm2, rs2, tS + (c + 1) * 16);
-            if (c + 2 < 4) ptx::tmem_wait_ld();
+            exp_chunk_regs(sb, sc2, nm2, rs2, mx, pw + (c + 1) * 16);
+            if (c + 2 < 4) ptx::tmem_wait_ld_regs(sa);
           }
         }
-        float rs0, rs1;
-        ptx::unpack2(rs2, rs0, rs1);
-        l_run += rs0 + rs1;
+        const float tmax = mx * sl2;               // this tile's row max (log2 domain)
+        if (j == 0 || tmax > m_run + kLazyMax) {
+          // redo the tile against its true max (S is still intact in TMEM)
+          const float mnew = fmaxf(m_run, tmax);
+          if (j > 0) {  // compose with a rescale still pending from the previous tile
+            alpha_pending = (rescale_pending ? alpha_pending : 1.f) * ptx::ex2(m_run - mnew);
+            rescale_pending = true;
+          }
+          m_run = mnew;
+          const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+          const uint64_t sc2 = ptx::pack2(sl2, sl2);
+          const uint64_t nm2 = ptx::pack2(-mref, -mref);
+          rs2 = 0ull;
+          float mdummy = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sa[32];
+            ptx::tmem_ld32(tS + c * 32, sa);
+            ptx::tmem_wait_ld_regs(sa);
+            if (diag) mask_chunk(sa, nvis - c * 32);
+            exp_chunk_regs(sa, sc2, nm2, rs2, mdummy, pw + c * 16);
+          }
+        }
+        // Apply a pending rescale of O (S_j being complete implies PV_{j-1}
+        // has completed: same issuing thread, in order).  TMEM loads/stores are
+        // warp-collective, so the whole warp takes the branch if any of its
+        // rows needs it (the others scale by 1).
+        if (__any_sync(0xffffffffu, rescale_pending)) {
+          const float alpha = rescale_pending ? alpha_pending : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + c * 32, o);
+            ptx::tmem_wait_ld_regs(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(tO + c * 32, o);
+          }
+          if (rescale_pending) l_run *= alpha;
+          rescale_pending = false;
+        }
+        {
+          float rs0, rs1;
+          ptx::unpack2(rs2, rs0, rs1);
+          l_run += rs0 + rs1;
+        }
+        // move the reference when the max grew by more than 2^8: takes effect
+        // for the next tile (O and l are rescaled before its PV)
+        if (j > 0 && tmax > m_run + kRescaleThreshold) {
+          const float mnew = tmax;
+          alpha_pending = ptx::ex2(m_run - mnew);
+          rescale_pending = true;
+          // this tile's P (already relative to the old m_run) joins O before
+          // the rescale, and its sum joins l before the rescale too
+          m_run = mnew;
+        }
+        // P over the first 64 columns of S (bf16 pairs)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w16[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) w16[h] = pw[c * 16 + h];
+          ptx::tmem_st16(tS + c * 16, w16);
+        }
         // Cache slots at or past ctx in the last page may hold anything (NaN
         // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
         // runs.  Both warpgroups may write the same zeros; rows past the last
@@ -493,7 +520,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         ptx::tmem_ld32(tO + c * 32, o);
-        ptx::tmem_wait_ld();
+        ptx::tmem_wait_ld_regs(o);
         if (row_valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
