@@ -43,8 +43,8 @@ namespace {
 constexpr int kPage = 16;
 constexpr int BM = 128;          // rows per query tile
 constexpr int BN = 128;          // keys per KV tile (8 pages)
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // MMA issuers: warps 9 and 10
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLazyMax = 64.0f;          // log2 units: largest tolerated P exponent
 
@@ -53,6 +53,7 @@ struct ChunkCfg {
   static constexpr int PANELS = D / 64;          // 128-byte swizzle panels along head_dim
   static constexpr int Q_BYTES = BM * D * 2;     // one query tile
   static constexpr int KV_BYTES = BN * D * 2;    // one K (or V) tile
+  static constexpr int PAGE_BYTES = 16 * D * 2;  // one page of one kv head
   static constexpr int KST = 3, VST = 2;       // K and V ring depths
   static constexpr int OFF_Q = 0;                // two query tiles
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
@@ -65,6 +66,7 @@ struct Bars {
   uint64_t q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
       o_final[2];
   uint32_t tmem_base;
+  uint32_t mma_lock;  // held by the issuer queueing a batch of MMAs
 };
 
 __device__ __forceinline__ int seq_work(const AttnParams &p, int s, int G) {
@@ -148,18 +150,19 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
 }
 
 // p = exp2(s * scale - m) for 32 columns, kept as bf16 pairs in `pw` (16
-// words); fp32 row sum accumulated in `rs2` (packed pair); raw max of s in mx.
+// words).  The fp32 row sum (packed pairs) and the raw max of s go to four
+// independent accumulators each, so neither is one long dependency chain.
 __device__ __forceinline__ void exp_chunk_regs(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
-                                               uint64_t &rs2, float &mx, uint32_t *pw) {
+                                               uint64_t (&rs2)[4], float (&mx)[4], uint32_t *pw) {
 #pragma unroll
   for (int h = 0; h < 16; ++h) {
     const float s0 = __uint_as_float(sr[2 * h]), s1 = __uint_as_float(sr[2 * h + 1]);
-    mx = ptx::max3(mx, s0, s1);
+    mx[h & 3] = ptx::max3(mx[h & 3], s0, s1);
     const uint64_t x2 = ptx::ffma2(ptx::pack2(s0, s1), sc2, nm2);
     float x0, x1;
     ptx::unpack2(x2, x0, x1);
     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-    rs2 = ptx::fadd2(rs2, ptx::pack2(p0, p1));
+    rs2[h & 3] = ptx::fadd2(rs2[h & 3], ptx::pack2(p0, p1));
     pw[h] = ptx::pack_bf16x2(p0, p1);
   }
 }
@@ -185,19 +188,20 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
 
   if (tid == 0) {
     ptx::mbar_init(&bs->q_full, 1);
-    ptx::mbar_init(&bs->q_empty, 1);
+    ptx::mbar_init(&bs->q_empty, 2);
     for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&bs->k_full[i], 1);
-      ptx::mbar_init(&bs->k_empty[i], 1);
+      ptx::mbar_init(&bs->k_empty[i], 2);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bs->v_full[i], 1);
-      ptx::mbar_init(&bs->v_empty[i], 1);
+      ptx::mbar_init(&bs->v_empty[i], 2);
       ptx::mbar_init(&bs->s_full[i], 1);
       ptx::mbar_init(&bs->p_full[i], 128);
       ptx::mbar_init(&bs->o_final[i], 1);
     }
     ptx::fence_mbar_init();
+    bs->mma_lock = 0u;
   }
   if (warp == kMmaWarp) ptx::tmem_alloc(&bs->tmem_base, 512);
   ptx::tc_fence_before();
@@ -244,7 +248,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       };
       // V lags K by one tile, so the block before the current one is kept too
       int blk_prev = kv_rows, blk_cur = load_block(0), blk_next = load_block(1), blk = 0;
-      auto load_tile = [&](unsigned char *dst, const CUtensorMap *tm, uint64_t *bar, int j) {
+      auto load_tile = [&](unsigned char *dst, bool is_v, uint64_t *bar, int j) {
         const int b = j >> 2;
         while (blk < b) {  // warp-uniform
           blk_prev = blk_cur;
@@ -258,11 +262,18 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, src, (j & 3) * 8 + i);
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar, C::KV_BYTES);
+          if (is_v) {
+            // V page-major: one box per page holds all its panels
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i)
+              ptx::tma_load_3d(dst + i * C::PAGE_BYTES, &tm_v, 0, rows[i], 0, bar);
+          } else {
 #pragma unroll
-            for (int pl = 0; pl < C::PANELS; ++pl)
-              ptx::tma_load_2d(dst + pl * BN * 128 + i * kPage * 128, tm, pl * 64, rows[i], bar);
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+              for (int pl = 0; pl < C::PANELS; ++pl)
+                ptx::tma_load_2d(dst + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i], bar);
+          }
         }
       };
       // K runs one tile ahead of V: K_t, then V_{t-1}
@@ -273,7 +284,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             ok = false;
             break;
           }
-          load_tile(sK + st * C::KV_BYTES, &tm_k, &bs->k_full[st], t);
+          load_tile(sK + st * C::KV_BYTES, false, &bs->k_full[st], t);
         }
         if (t >= 1) {
           const uint32_t vc = kvc + t - 1, st = vc % C::VST;
@@ -281,85 +292,136 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             ok = false;
             break;
           }
-          load_tile(sV + st * C::KV_BYTES, &tm_v, &bs->v_full[st], t - 1);
+          load_tile(sV + st * C::KV_BYTES, true, &bs->v_full[st], t - 1);
         }
       }
       kvc += it.n_kv;
     }
     if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
-  } else if (warp == kMmaWarp) {
-    // ------------------------------- MMA issuer ---------------------------------
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------ MMA issuers --------------------------------
+    // One issuing thread per query tile slot (warp 9: tile 0, warp 10: tile 1).
+    // Issuing a tcgen05.mma stalls while the tensor pipe's queue is full, so a
+    // single issuer for both tiles would notice one tile's P only after it got
+    // the other tile's MMAs queued.  A commit tracks the issuing thread's own
+    // operations, which is what each tile's s_full / o_final need.  The K/V
+    // stage and Q release barriers take one arrival per tile: a tile that reads
+    // a stage the other tile does not read (the later tile sees more keys; the
+    // second tile may be absent) commits twice, so both arrivals come after
+    // its reads.  Both issuers wait on q_full for every item, so neither ever
+    // skips a phase of it.
+    const int ti = warp - kMmaWarp;
+    // A tile's batch (PV_j and the next QK^T) enters the tensor pipe as a
+    // whole: interleaved one MMA at a time, both tiles' S would complete
+    // together and their softmaxes would run together instead of each one
+    // overlapping the other tile's MMAs.
+    auto lock = [&]() -> bool {
+      for (uint32_t i = 0; i < (1u << 22); ++i) {
+        if (atomicCAS(&bs->mma_lock, 0u, 1u) == 0u) return true;
+        __nanosleep(32);
+      }
+      return false;
+    };
+    auto unlock = [&]() { atomicExch(&bs->mma_lock, 0u); };
     constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
     constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
-    uint32_t kvm = 0;             // K/V tiles consumed so far by this CTA
-    uint32_t pcnt0 = 0, pcnt1 = 0;  // P tiles consumed per query tile slot
+    const uint32_t tS = tmem + ti * 128, tO = tmem + 256 + ti * 128;
+    // Every shared-memory descriptor this issuer uses, built once: the issuing
+    // warp shares its scheduler with two softmax warps, so each instruction
+    // between MMAs costs several cycles and delays the tensor pipe's queue.
+    constexpr int KS = D / 16, VS = BN / 16;
+    uint64_t qdesc[KS], kdesc[C::KST][KS], vdesc[C::VST][VS];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int o = (ks >> 2) * BM * 128 + (ks & 3) * 32;  // panel, 16-element step
+      qdesc[ks] = ptx::smem_desc_sw128(sQ + ti * C::Q_BYTES + o, 16, 1024);
+#pragma unroll
+      for (int st = 0; st < C::KST; ++st)
+        kdesc[st][ks] = ptx::smem_desc_sw128(sK + st * C::KV_BYTES + o, 16, 1024);
+    }
+#pragma unroll
+    for (int st = 0; st < C::VST; ++st)
+#pragma unroll
+      for (int ks = 0; ks < VS; ++ks)
+        vdesc[st][ks] = ptx::smem_desc_sw128(sV + st * C::KV_BYTES + ks * C::PAGE_BYTES,
+                                             kPage * 128, 1024);
+    uint32_t kvm = 0;   // K/V tiles loaded so far for this CTA (both tiles agree)
+    uint32_t pcnt = 0;  // P tiles of this slot consumed
     bool ok = true;
     int n = 0;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
       Item it;
       if (!warp_find_item<G>(p, item, it)) break;
       if (lane == 0) {
-        auto issue_qk = [&](int i, uint32_t kvidx) {
-          const unsigned char *kk = sK + (kvidx % C::KST) * C::KV_BYTES;
-          const unsigned char *qq = sQ + i * C::Q_BYTES;
+        const int n_mine = ti ? it.n_kv1 : it.n_kv0;
+        const int n_other = ti ? it.n_kv0 : it.n_kv1;
+        // QK^T MMAs only; the caller commits
+        auto issue_qk = [&](uint32_t kvidx) {
+          const uint32_t st = kvidx % C::KST;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const int pl = ks >> 2, within = (ks & 3) * 32;
-            const uint64_t a = ptx::smem_desc_sw128(qq + pl * BM * 128 + within, 16, 1024);
-            const uint64_t b = ptx::smem_desc_sw128(kk + pl * BN * 128 + within, 16, 1024);
-            ptx::mma_bf16_ss(tmem + i * 128, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          for (int s3 = 0; s3 < C::KST; ++s3) {
+            if (st == (uint32_t)s3) {
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+                ptx::mma_bf16_ss(tS, qdesc[ks], kdesc[s3][ks], idesc_qk, ks > 0 ? 1u : 0u);
+            }
           }
-          ptx::mma_commit(&bs->s_full[i]);
         };
-        ok = ptx::mbar_wait(&bs->q_full, n & 1) &&
-             ptx::mbar_wait(&bs->k_full[kvm % C::KST], (kvm / C::KST) & 1);
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_qk(0, kvm);
-          if (it.n_kv1 > 0) issue_qk(1, kvm);
-          ptx::mma_commit(&bs->k_empty[kvm % C::KST]);
+        auto release_k = [&](uint32_t kvidx) {
+          ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
+          if ((int)(kvidx - kvm) >= n_other) ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
+        };
+        ok = ptx::mbar_wait(&bs->q_full, n & 1);
+        if (ok && n_mine > 0) {
+          ok = ptx::mbar_wait(&bs->k_full[kvm % C::KST], (kvm / C::KST) & 1) && lock();
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_qk(kvm);
+            unlock();
+            ptx::mma_commit(&bs->s_full[ti]);
+            release_k(kvm);
+          }
         }
-        for (int j = 0; ok && j < it.n_kv; ++j) {
+        for (int j = 0; ok && j < n_mine; ++j) {
           const uint32_t kv = kvm + j;
           const int vst = kv % C::VST;
-          bool v_ready = false, k_next_ready = false;
-          for (int i = 0; ok && i < 2; ++i) {
-            const int n_i = i ? it.n_kv1 : it.n_kv0;
-            if (j >= n_i) continue;
-            const uint32_t pc = i ? pcnt1 : pcnt0;
-            if (!ptx::mbar_wait(&bs->p_full[i], pc & 1)) { ok = false; break; }
-            if (i) ++pcnt1; else ++pcnt0;
-            if (!v_ready) {
-              if (!ptx::mbar_wait(&bs->v_full[vst], (kv / C::VST) & 1)) { ok = false; break; }
-              v_ready = true;
-            }
-            ptx::tc_fence_after();
-            const unsigned char *vv = sV + vst * C::KV_BYTES;
+          const bool more = j + 1 < n_mine;
+          // everything the batch reads is resident before it starts, so its
+          // MMAs go to the tensor pipe back to back; the commits follow them
+          if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) ||
+              !ptx::mbar_wait(&bs->v_full[vst], (kv / C::VST) & 1) ||
+              (more && !ptx::mbar_wait(&bs->k_full[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) ||
+              !lock()) {
+            ok = false;
+            break;
+          }
+          ++pcnt;
+          ptx::tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < BN / 16; ++ks) {
-              const uint64_t b = ptx::smem_desc_sw128(vv + ks * 16 * 128, BN * 128, 1024);
-              ptx::mma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + ks * 8, b, idesc_pv,
-                               (j > 0 || ks > 0) ? 1u : 0u);
-            }
-            if (j + 1 < n_i) {
-              if (!k_next_ready) {
-                if (!ptx::mbar_wait(&bs->k_full[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) {
-                  ok = false;
-                  break;
-                }
-                k_next_ready = true;
-                ptx::tc_fence_after();
-              }
-              issue_qk(i, kv + 1);
-            } else {
-              ptx::mma_commit(&bs->o_final[i]);
+          for (int s2 = 0; s2 < C::VST; ++s2) {
+            if (vst == s2) {
+#pragma unroll
+              for (int ks = 0; ks < VS; ++ks)
+                ptx::mma_bf16_ts(tO, tS + ks * 8, vdesc[s2][ks], idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
             }
           }
-          // V_j has no later reader; K_{j+1} was last read by this iteration's QKs
+          if (more) issue_qk(kv + 1);
+          // the batch is queued: the other tile may queue its own behind it
+          // while this thread's commits wait for these MMAs
+          unlock();
+          if (more) {
+            ptx::mma_commit(&bs->s_full[ti]);
+            release_k(kv + 1);
+          } else {
+            ptx::mma_commit(&bs->o_final[ti]);
+          }
           ptx::mma_commit(&bs->v_empty[vst]);
-          if (k_next_ready) ptx::mma_commit(&bs->k_empty[(kv + 1) % C::KST]);
+          if (j >= n_other) ptx::mma_commit(&bs->v_empty[vst]);
         }
-        ptx::mma_commit(&bs->q_empty);
+        if (ok && n_mine > 0) {
+          ptx::mma_commit(&bs->q_empty);
+          if (n_other == 0) ptx::mma_commit(&bs->q_empty);
+        }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       kvm += it.n_kv;
@@ -401,9 +463,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         // it grew by more than 2^8; a tile whose max jumps by more than
         // 2^kLazyMax, and the first tile, are redone against their true max.
         uint32_t pw[BN / 2];
-        float mx = -INFINITY;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const float mref0 = (j == 0) ? INFINITY : m_run;  // first tile: no reference yet
-        uint64_t rs2 = 0ull;
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
         {
           const uint64_t sc2 = ptx::pack2(sl2, sl2);
           const uint64_t nm2 = ptx::pack2(-mref0, -mref0);
@@ -422,7 +484,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             if (c + 2 < 4) ptx::tmem_wait_ld_regs(sa);
           }
         }
-        const float tmax = mx * sl2;               // this tile's row max (log2 domain)
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // tile row max (log2)
         if (j == 0 || tmax > m_run + kLazyMax) {
           // redo the tile against its true max (S is still intact in TMEM)
           const float mnew = fmaxf(m_run, tmax);
@@ -434,8 +496,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           const float mref = (m_run == -INFINITY) ? 0.f : m_run;
           const uint64_t sc2 = ptx::pack2(sl2, sl2);
           const uint64_t nm2 = ptx::pack2(-mref, -mref);
-          rs2 = 0ull;
-          float mdummy = -INFINITY;
+#pragma unroll
+          for (int a = 0; a < 4; ++a) rs2[a] = 0ull;
+          float mdummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t sa[32];
@@ -464,8 +527,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           rescale_pending = false;
         }
         {
+          const uint64_t r2 = ptx::fadd2(ptx::fadd2(rs2[0], rs2[1]), ptx::fadd2(rs2[2], rs2[3]));
           float rs0, rs1;
-          ptx::unpack2(rs2, rs0, rs1);
+          ptx::unpack2(r2, rs0, rs1);
           l_run += rs0 + rs1;
         }
         // move the reference when the max grew by more than 2^8: takes effect
@@ -494,12 +558,13 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           const uint32_t kv = kvb + j;
           if (!ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1)) { ok = false; break; }
           if (r >= ctx - key0 && r < it.n_pages * kPage - key0) {
-            unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + r * 128;
+            unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + (r / kPage) * C::PAGE_BYTES +
+                                  (r % kPage) * 128;
 #pragma unroll
             for (int pl = 0; pl < C::PANELS; ++pl)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(vrow + pl * BN * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(vrow + pl * kPage * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
           ptx::fence_proxy_async_smem();
         }
@@ -581,14 +646,28 @@ cudaError_t launch_dg(const AttnParams &p, int grid, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   const int64_t rows = p.num_pages * p.Hkv * kPage;
-  for (int which = 0; which < 2; ++which) {
+  {
+    // K: cache rows [rows][D], box = one 64-dim panel of one page (16 rows)
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)D * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)kPage};
     cuuint32_t estr[2] = {1, 1};
-    if (encode(which == 0 ? &tk : &tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-               const_cast<void *>(which == 0 ? p.k_cache : p.v_cache), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.k_cache), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // V: the same rows viewed as (64 dims, row, panel), box = a whole page with
+    // its panels outermost, i.e. [panel][16 rows][64 dims] in shared memory --
+    // each page is exactly the B operand of one 16-key step of PV.
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)C::PANELS};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kPage, (cuuint32_t)C::PANELS};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.v_cache), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
