@@ -449,7 +449,9 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       float m_run = -INFINITY, l_run = 0.f, alpha_pending = 1.f;
       bool rescale_pending = false;
       for (int j = 0; j < n_mine; ++j, ++scnt) {
-        if (!ptx::mbar_wait(&bs->s_full[ti], scnt & 1)) { ok = false; break; }
+        // waits are combined over the warp so a timeout never splits it
+        // before a warp-collective TMEM access
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->s_full[ti], scnt & 1))) { ok = false; break; }
         ptx::tc_fence_after();
         const int key0 = j * BN;
         const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
@@ -485,10 +487,14 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           }
         }
         const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // tile row max (log2)
-        if (j == 0 || tmax > m_run + kLazyMax) {
-          // redo the tile against its true max (S is still intact in TMEM)
-          const float mnew = fmaxf(m_run, tmax);
-          if (j > 0) {  // compose with a rescale still pending from the previous tile
+        // Redo the tile against its true max (S is still intact in TMEM).  The
+        // TMEM loads are warp-collective, so the warp redoes the tile if any
+        // of its rows needs it; for the other rows the reference is unchanged
+        // and the recomputed P equals the first one.
+        const bool redo = (j == 0) || (tmax > m_run + kLazyMax);
+        if (__any_sync(0xffffffffu, redo)) {
+          const float mnew = redo ? fmaxf(m_run, tmax) : m_run;
+          if (j > 0 && redo) {  // compose with a rescale still pending from the previous tile
             alpha_pending = (rescale_pending ? alpha_pending : 1.f) * ptx::ex2(m_run - mnew);
             rescale_pending = true;
           }
@@ -556,7 +562,10 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         // page were loaded out of range and are zero already.
         if (key0 + BN > ctx) {
           const uint32_t kv = kvb + j;
-          if (!ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1))) {
+            ok = false;
+            break;
+          }
           if (r >= ctx - key0 && r < it.n_pages * kPage - key0) {
             unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + (r / kPage) * C::PAGE_BYTES +
                                   (r % kPage) * 128;
@@ -575,7 +584,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       kvb += it.n_kv;
       if (!ok || n_mine == 0) continue;
       // epilogue: O / l
-      if (!ptx::mbar_wait(&bs->o_final[ti], ocnt & 1)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->o_final[ti], ocnt & 1))) { ok = false; break; }
       ++ocnt;
       ptx::tc_fence_after();
       const float inv = 1.f / l_run;

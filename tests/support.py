@@ -59,10 +59,12 @@ def oracle_state_for(ws):
 
 
 def make_step(q_lens, seq_lens, Hq, Hkv, D, dtype, seed, page_size=16,
-              pool_factor=1.5, device="cpu"):
+              pool_factor=1.5, device="cpu", transform=None):
     """A one-step problem on CPU: per-position Q/K/V from the generator, pages
     from a random permutation, the package's metadata, and the logical
-    (unpaged) K/V of each sequence for the dense oracle."""
+    (unpaged) K/V of each sequence for the dense oracle.  ``transform(q,
+    k_seqs, v_seqs)`` may return edited tensors before anything is derived
+    from them (planted structure for special cases)."""
     st = synth.draw_sequences(seq_lens, [s - q for q, s in zip(q_lens, seq_lens)],
                               Hq, Hkv, D, dtype, seed)
     need = sum(pages_for(s, page_size) for s in seq_lens)
@@ -74,6 +76,8 @@ def make_step(q_lens, seq_lens, Hq, Hkv, D, dtype, seed, page_size=16,
     k_seqs = [st.k[o:o + L] for o, L in zip(st.kv_offsets, seq_lens)]
     v_seqs = [st.v[o:o + L] for o, L in zip(st.kv_offsets, seq_lens)]
     q = st.q
+    if transform is not None:
+        q, k_seqs, v_seqs = transform(q, k_seqs, v_seqs)
     new_k = torch.cat([ks[L - ql:] for ks, L, ql in zip(k_seqs, seq_lens, q_lens)])
     new_v = torch.cat([vs[L - ql:] for vs, L, ql in zip(v_seqs, seq_lens, q_lens)])
     # oracle-side cache: prefix via the oracle's own slots, then the new rows

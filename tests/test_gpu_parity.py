@@ -129,6 +129,48 @@ def test_small_hybrid_batches(cuda_device, case):
     assert_close(out.cpu(), want, f"case {case}")
 
 
+def _planted_logit_jumps(q, k_seqs, v_seqs):
+    """Sequence 0 (a chunk): every query row is one direction u per kv-head
+    group; the first key tile is near-orthogonal (logits ~0), keys 128..191
+    are 1.0 u (a jump of ~16 in log2 units: the running max moves) and keys
+    384..447 are 5.0 u (a jump of ~80: past the lazy bound, the tile is
+    recomputed against its own max)."""
+    q, k0 = q.clone(), k_seqs[0].clone()
+    T0 = k0.shape[0]
+    q_len0 = 100
+    Hq, D = q.shape[1], q.shape[2]
+    Hkv = k0.shape[1]
+    G = Hq // Hkv
+    gen = torch.Generator().manual_seed(4242)
+    u = torch.randn(Hkv, D, generator=gen)
+    q[:q_len0] = u.repeat_interleave(G, dim=0).to(q.dtype)[None]
+    k0 = (k0.float() * 0.05).to(k0.dtype)
+    k0[128:192] = u.to(k0.dtype)[None]
+    k0[384:448] = (5.0 * u).to(k0.dtype)[None]
+    assert T0 > 448
+    return q, [k0] + list(k_seqs[1:]), v_seqs
+
+
+def test_large_logit_jumps_rescale_and_redo(cuda_device):
+    q_lens, seq_lens = [100, 1], [800, 900]
+    Hq, Hkv, D = 32, 8, 128
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=77,
+                   transform=_planted_logit_jumps)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(D)
+    out, _ = gpu_step(k_cache, v_cache, inp, scale, Hq)
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    # the planted keys dominate: the output is close to the mean of their V rows
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    assert_close(out.cpu(), want, "planted logit jumps")
+
+
 DECODE_CASES = [
     # (num decodes, ctx range, Hq, Hkv, D) -- decode kernel shapes and fallbacks
     (3, (1, 40), 8, 4, 128),       # fewer pages than workers, ragged pages
