@@ -392,6 +392,75 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+
+def run_sweep(args):
+    """Budget sweep: an 8192-token prompt prefilled from scratch beside 32
+    decodes, once per token budget, every step timed (append + attention, L2
+    flushed before each); per budget the mean step time, the prompt's total
+    prefill time and the mean fraction of each step's roofline."""
+    from chunked_prefill_paged_cpa_gb300 import ops, workloads
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    ops.load()
+    peaks, peak_src = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    rows = []
+    for budget in (256, 512, 2048, 16384):
+        sc = workloads.budget_sweep(budget, args.seed)
+        ws = workloads.WorkloadState(sc, device=dev)
+        sh = sc.shape
+        eb = torch.empty((), dtype=sh.dtype).element_size()
+        steps = [ws.step(k) for k in range(len(sc.plans))]
+        max_pages = max(s["meta"].block_table.shape[1] for s in steps)
+        max_seqs = max(s["meta"].num_seqs for s in steps)
+        wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, max_pages, max_seqs)
+        outs = [torch.empty_like(s["q"]) for s in steps]
+
+        def one(k):
+            s, m = steps[k], steps[k]["meta"]
+            ops.kv_append(s["k"], s["v"], m.slot_mapping, ws.k_cache, ws.v_cache, stream=stream)
+            ops.attention_forward(s["q"], ws.k_cache, ws.v_cache, m.block_table,
+                                  m.query_start_loc, m.seq_lens, sh.scale, wsp, out=outs[k],
+                                  stream=stream)
+
+        for k in range(len(steps)):       # warm-up pass (appends are idempotent)
+            one(k)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in steps]
+        for k in range(len(steps)):
+            flush.fill_(k & 0xff)
+            ev[k][0].record(stream)
+            one(k)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        fr = []
+        for k, s in enumerate(steps):
+            m = s["meta"]
+            c = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads,
+                            sh.head_dim, eb)
+            roof = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9), c["flops"] / (peaks["bf16_tflops"] * 1e12))
+            fr.append(roof * 1e6 / us[k])
+        rows.append({"budget": budget, "steps": len(steps), "chunk_tokens": budget - 32,
+                     "step_us_mean": sum(us) / len(us), "step_us_max": max(us),
+                     "prompt_prefill_ms": sum(us) / 1e3,
+                     "decode_tokens_during_prefill": 32 * len(steps),
+                     "step_roofline_frac_mean": sum(fr) / len(fr)})
+        del ws, steps, outs, wsp
+        torch.cuda.empty_cache()
+    line = {"metric": "budget sweep: per-step us and total prompt prefill time", "unit": "us",
+            "higher_is_better": False, "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "budget_sweep", "prompt": 8192, "decodes": 32,
+                       "decode_context": "U[512, 4096]", "heads": "32q/8kv", "head_dim": 128,
+                       "page_size": 16, "seed": args.seed,
+                       "l2": "flushed before every timed step",
+                       "peaks": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"},
+            "sweep": rows}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -403,7 +472,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=15.0,
                     help="seconds of host work per oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="budget sweep of an 8192-token prompt beside 32 decodes (one JSON line)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -33,7 +33,7 @@ import torch
 
 from . import synth
 from .batch import PageAllocator, PagedSeqs, build_metadata, write_positions, pages_for
-from .sched import Request, StepPlan, commit, schedule_step
+from .sched import BudgetError, Request, StepPlan, commit, schedule_step
 
 
 @dataclass
@@ -116,6 +116,20 @@ def scenario(name: str, seed: int = 0) -> Scenario:
         L = synth.uniform_lengths(256, 2048, 8192, s_len)
         return _run(name, LLAMA3_8B, _decoders(L), [], 256, 1, seed, {"budget": 256})
     raise KeyError(name)
+
+
+def budget_sweep(budget: int, seed: int = 0, prompt: int = 8192, decodes: int = 32) -> Scenario:
+    """An ``prompt``-token prompt prefilled from scratch beside ``decodes``
+    running decodes (contexts ~U[512, 4096]) under a token budget, stepped until
+    its prefill completes: decode-first composition gives each step
+    ``budget - decodes`` prompt tokens ("Chunked Prefill" (deepconcepts.dev),
+    "Why a chunk can be nearly free", the budget sweep of its simulation)."""
+    if budget <= decodes:
+        raise BudgetError("budget must exceed the number of running decodes")
+    L = synth.uniform_lengths(decodes, 512, 4096, seed * 1000 + 1)
+    steps = -(-prompt // (budget - decodes))
+    return _run(f"budget_sweep_{budget}", LLAMA3_8B, _decoders(L), [Request("P", prompt, 0)],
+                budget, steps, seed, {"budget": budget, "prompt": prompt, "decodes": decodes})
 
 
 NAMES = ["tiny", "page1_default", "large_budget", "long_context", "decode_only"]
