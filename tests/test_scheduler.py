@@ -113,3 +113,18 @@ def test_chunked_scenario_covers_prompt():
     chunks = [[s for s in p.seqs if s.rid == "P"] for p in sc.plans]
     assert [(c[0].q_len, c[0].seq_len) for c in chunks] == [
         (2048, 2048), (2048, 4096), (2048, 6144), (2048, 8192)]
+
+
+def test_budget_sweep_scenarios_cover_the_prompt():
+    from chunked_prefill_paged_cpa_gb300 import workloads
+    for budget, steps in ((256, 37), (512, 18), (2048, 5), (16384, 1)):
+        sc = workloads.budget_sweep(budget)
+        assert len(sc.plans) == steps
+        chunks = [s.q_len for p in sc.plans for s in p.seqs if s.rid == "P"]
+        assert sum(chunks) == 8192
+        # decode-first: every step carries the 32 decodes and a chunk of the rest
+        for p in sc.plans:
+            assert sum(1 for s in p.seqs if s.rid != "P") == 32
+            assert sum(s.q_len for s in p.seqs) <= budget
+    with pytest.raises(Exception):
+        workloads.budget_sweep(32)
