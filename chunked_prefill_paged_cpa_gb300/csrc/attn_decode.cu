@@ -36,6 +36,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kPage = 16;
+constexpr float kLazyRescale = 8.0f;  // log2 units
 
 template <int D>
 struct Cfg {
@@ -314,13 +315,16 @@ attn_decode_kernel(const AttnParams p) {
 #pragma unroll
       for (int r = 0; r < G; ++r)
         pmax[r] = ((r / HALF) == b0) ? mine[r % HALF] : theirs[r % HALF];
-      // online softmax update (per 8-lane group; all lanes of a group agree)
+      // online softmax update (per 8-lane group; all lanes of a group agree).
+      // The reference m only moves when the max grew by more than 2^8 (or at
+      // the first visible key), so p stays below 2^8 and O is rescaled rarely.
       float alpha[G];
       bool any_rescale = false;
 #pragma unroll
       for (int r = 0; r < G; ++r) {
-        const float mn = fmaxf(m[r], pmax[r]);
-        alpha[r] = (mn == -INFINITY) ? 1.f : exp2f(m[r] - mn);
+        const bool move = pmax[r] > m[r] + kLazyRescale;  // m = -inf: any visible key
+        const float mn = move ? pmax[r] : m[r];
+        alpha[r] = (move && m[r] != -INFINITY) ? ptx::ex2(m[r] - mn) : 1.f;
         any_rescale |= (alpha[r] != 1.f);
         m[r] = mn;
       }
@@ -328,7 +332,7 @@ attn_decode_kernel(const AttnParams p) {
       for (int j = 0; j < HALF; ++j) {
         const float mj = b0 ? m[HALF + j] : m[j];
         const float aj = b0 ? alpha[HALF + j] : alpha[j];
-        const float pj = (mj == -INFINITY) ? 0.f : exp2f(sv[j] - mj);
+        const float pj = (mj == -INFINITY) ? 0.f : ptx::ex2(sv[j] - mj);
         lpart[j] = lpart[j] * aj + pj;
         pbuf[myk * G + r0 + j] = pj;
       }
@@ -394,7 +398,7 @@ attn_decode_kernel(const AttnParams p) {
         float mx = m[r];
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float sc = (m[r] == -INFINITY) ? 0.f : exp2f(m[r] - mx);
+        const float sc = (m[r] == -INFINITY) ? 0.f : ptx::ex2(m[r] - mx);
         float l = lg[r] * sc;
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
@@ -479,7 +483,7 @@ attn_decode_kernel(const AttnParams p) {
             float lsum = 0.f;
             for (int c = lane; c < nc; c += 32) {
               const float2 ml = __ldcg(&p.part_ml[(base + c) * G + r]);
-              lsum += (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - mx);
+              lsum += (ml.x == -INFINITY) ? 0.f : ml.y * ptx::ex2(ml.x - mx);
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
@@ -494,7 +498,7 @@ attn_decode_kernel(const AttnParams p) {
               for (int u = 0; u < 8; ++u) {
                 const int c = min(c0 + u, nc - 1);
                 const float mc = __ldcg(&p.part_ml[(base + c) * G + r].x);
-                wgt[u] = (c0 + u < nc && mc != -INFINITY) ? exp2f(mc - mx) : 0.f;
+                wgt[u] = (c0 + u < nc && mc != -INFINITY) ? ptx::ex2(mc - mx) : 0.f;
                 const float *src = p.part_o + ((base + c) * G + r) * D + lane * DPL;
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) ov[u][e] = __ldcg(src + e);
