@@ -281,7 +281,22 @@ def run_gpu(args, world, rank, local):
         flush.fill_(1)
         step()
     torch.cuda.synchronize()
-    launches_per_step = 2
+    # this library's kernels per step, as cpa_attention_forward dispatches
+    # them: the append, then the chunk-tile kernel (bf16, head_dim 64/128, GQA
+    # 1/2/4/8) when the step has chunks, the streaming decode kernel (bf16,
+    # GQA 2/4/8, group * head_dim <= 512) whenever that path applies, and the
+    # row kernel for whatever neither takes
+    G = sh.num_q_heads // sh.num_kv_heads
+    bf16 = sh.dtype == torch.bfloat16 and sh.head_dim in (64, 128)
+    fast_decode = bf16 and G in (2, 4, 8) and G * sh.head_dim <= 512
+    all_decode = all(q == 1 for q in m.q_lens)
+    launch_chunks = bf16 and G in (1, 2, 4, 8) and not all_decode
+    if launch_chunks and fast_decode:
+        attn_launches = 2
+    else:
+        rows = (not fast_decode) or (not all_decode and not launch_chunks)
+        attn_launches = int(fast_decode) + int(launch_chunks) + int(rows)
+    launches_per_step = 1 + attn_launches
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier(world)
