@@ -492,6 +492,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         // of its rows needs it; for the other rows the reference is unchanged
         // and the recomputed P equals the first one.
         const bool redo = (j == 0) || (tmax > m_run + kLazyMax);
+        bool p_stored = false;  // warp-uniform
         if (__any_sync(0xffffffffu, redo)) {
           const float mnew = redo ? fmaxf(m_run, tmax) : m_run;
           if (j > 0 && redo) {  // compose with a rescale still pending from the previous tile
@@ -505,14 +506,19 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int a = 0; a < 4; ++a) rs2[a] = 0ull;
           float mdummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
+          // A rolled loop (this path runs once per item, and the unrolled
+          // body would compete for the instruction cache): each chunk's P goes
+          // straight to TMEM over S columns this loop has already read.
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
-            uint32_t sa[32];
+            uint32_t sa[32], w16[16];
             ptx::tmem_ld32(tS + c * 32, sa);
             ptx::tmem_wait_ld_regs(sa);
             if (diag) mask_chunk(sa, nvis - c * 32);
-            exp_chunk_regs(sa, sc2, nm2, rs2, mdummy, pw + c * 16);
+            exp_chunk_regs(sa, sc2, nm2, rs2, mdummy, w16);
+            ptx::tmem_st16(tS + c * 16, w16);
           }
+          p_stored = true;
         }
         // Apply a pending rescale of O (S_j being complete implies PV_{j-1}
         // has completed: same issuing thread, in order).  TMEM loads/stores are
@@ -549,12 +555,14 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
           m_run = mnew;
         }
         // P over the first 64 columns of S (bf16 pairs)
+        if (!p_stored) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w16[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w16[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) w16[h] = pw[c * 16 + h];
-          ptx::tmem_st16(tS + c * 16, w16);
+            for (int h = 0; h < 16; ++h) w16[h] = pw[c * 16 + h];
+            ptx::tmem_st16(tS + c * 16, w16);
+          }
         }
         // Cache slots at or past ctx in the last page may hold anything (NaN
         // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
