@@ -14,12 +14,12 @@
 //
 // Per CTA (320 threads, one CTA per SM):
 //   warps 0-3  softmax for tile 0, warps 4-7 softmax for tile 1; one thread
-//              per row.  One pass over S in TMEM: causal mask (diagonal
-//              tiles only), exp2 against the running max of the earlier tiles
-//              (log2 domain) while the tile's own max is tracked, row sum, and
-//              P in bf16 written back into TMEM over S.  The running max (and
-//              with it the TMEM O accumulator) moves only when it grew by more
-//              than 2^8; the first tile and a jump past 2^64 are redone.
+//              per row.  Two short rolled passes over S in TMEM: the tile's
+//              row max (causal mask on diagonal tiles only), then exp2 against
+//              the running max (log2 domain), row sum, and P in bf16 written
+//              back into TMEM over S chunk by chunk.  The running max (and with
+//              it the TMEM O accumulator) moves only when it grew by more than
+//              2^8.
 //   warp 8     TMA producer: both Q tiles (3-d tensor map over q, 128-byte
 //              swizzle), then per KV tile of BN = 128 keys the 8 pages of K
 //              and of V of kv head g (2-d tensor map over the cache rows);
@@ -46,7 +46,6 @@ constexpr int BN = 128;          // keys per KV tile (8 pages)
 constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // MMA issuers: warps 9 and 10
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr float kLazyMax = 64.0f;          // log2 units: largest tolerated P exponent
 
 template <int D>
 struct ChunkCfg {
@@ -149,16 +148,15 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
     if (e >= n) sr[e] = __float_as_uint(-INFINITY);
 }
 
-// p = exp2(s * scale - m) for 32 columns, kept as bf16 pairs in `pw` (16
-// words).  The fp32 row sum (packed pairs) and the raw max of s go to four
-// independent accumulators each, so neither is one long dependency chain.
+// p = exp2(s * scale - m) for 32 columns as 16 bf16 pairs in `pw`; the fp32
+// row sum (packed pairs) goes to four independent accumulators, so it is not
+// one long dependency chain.
 __device__ __forceinline__ void exp_chunk_regs(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
-                                               uint64_t (&rs2)[4], float (&mx)[4], uint32_t *pw) {
+                                               uint64_t (&rs2)[4], uint32_t (&pw)[16]) {
 #pragma unroll
   for (int h = 0; h < 16; ++h) {
-    const float s0 = __uint_as_float(sr[2 * h]), s1 = __uint_as_float(sr[2 * h + 1]);
-    mx[h & 3] = ptx::max3(mx[h & 3], s0, s1);
-    const uint64_t x2 = ptx::ffma2(ptx::pack2(s0, s1), sc2, nm2);
+    const uint64_t x2 = ptx::ffma2(ptx::pack2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])),
+                                   sc2, nm2);
     float x0, x1;
     ptx::unpack2(x2, x0, x1);
     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
@@ -446,8 +444,7 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       const int tok = (2 * it.mp + ti) * TM + r / G;  // index within the chunk
       const bool row_valid = tok < q_len;
       const int last = row_valid ? ctx - q_len + tok : 0;
-      float m_run = -INFINITY, l_run = 0.f, alpha_pending = 1.f;
-      bool rescale_pending = false;
+      float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_mine; ++j, ++scnt) {
         // waits are combined over the warp so a timeout never splits it
         // before a warp-collective TMEM access
@@ -456,76 +453,28 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         const int key0 = j * BN;
         const bool diag = key0 + BN - 1 > last;  // tile holds keys past `last`
         const int nvis = last - key0 + 1;        // visible keys of this row in the tile
-        // One pass over S (4 chunks of 32 columns, the next chunk's TMEM load in
-        // flight): p = exp2(S * scale - m_run) against the running max of the
-        // earlier tiles, kept in registers as bf16 pairs while this tile's own
-        // max is tracked.  P and the row sum stay finite as long as the tile
-        // max exceeds m_run by less than 2^kLazyMax (bf16 and fp32 both reach
-        // 2^127), so the running max is only moved -- O and l rescaled -- when
-        // it grew by more than 2^8; a tile whose max jumps by more than
-        // 2^kLazyMax, and the first tile, are redone against their true max.
-        uint32_t pw[BN / 2];
+        // Pass 1: the tile's row max (rolled; TMEM loads are cheap).
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        const float mref0 = (j == 0) ? INFINITY : m_run;  // first tile: no reference yet
-        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
-        {
-          const uint64_t sc2 = ptx::pack2(sl2, sl2);
-          const uint64_t nm2 = ptx::pack2(-mref0, -mref0);
-          uint32_t sa[32], sb[32];
-          ptx::tmem_ld32(tS, sa);
-          ptx::tmem_wait_ld_regs(sa);
-#pragma unroll
-          for (int c = 0; c < 4; c += 2) {
-            ptx::tmem_ld32(tS + (c + 1) * 32, sb);
-            if (diag) mask_chunk(sa, nvis - c * 32);
-            exp_chunk_regs(sa, sc2, nm2, rs2, mx, pw + c * 16);
-            ptx::tmem_wait_ld_regs(sb);
-            if (c + 2 < 4) ptx::tmem_ld32(tS + (c + 2) * 32, sa);
-            if (diag) mask_chunk(sb, nvis - (c + 1) * 32);
-            exp_chunk_regs(sb, sc2, nm2, rs2, mx, pw + (c + 1) * 16);
-            if (c + 2 < 4) ptx::tmem_wait_ld_regs(sa);
-          }
-        }
-        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // tile row max (log2)
-        // Redo the tile against its true max (S is still intact in TMEM).  The
-        // TMEM loads are warp-collective, so the warp redoes the tile if any
-        // of its rows needs it; for the other rows the reference is unchanged
-        // and the recomputed P equals the first one.
-        const bool redo = (j == 0) || (tmax > m_run + kLazyMax);
-        bool p_stored = false;  // warp-uniform
-        if (__any_sync(0xffffffffu, redo)) {
-          const float mnew = redo ? fmaxf(m_run, tmax) : m_run;
-          if (j > 0 && redo) {  // compose with a rescale still pending from the previous tile
-            alpha_pending = (rescale_pending ? alpha_pending : 1.f) * ptx::ex2(m_run - mnew);
-            rescale_pending = true;
-          }
-          m_run = mnew;
-          const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-          const uint64_t sc2 = ptx::pack2(sl2, sl2);
-          const uint64_t nm2 = ptx::pack2(-mref, -mref);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) rs2[a] = 0ull;
-          float mdummy[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          // A rolled loop (this path runs once per item, and the unrolled
-          // body would compete for the instruction cache): each chunk's P goes
-          // straight to TMEM over S columns this loop has already read.
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sa[32], w16[16];
-            ptx::tmem_ld32(tS + c * 32, sa);
-            ptx::tmem_wait_ld_regs(sa);
-            if (diag) mask_chunk(sa, nvis - c * 32);
-            exp_chunk_regs(sa, sc2, nm2, rs2, mdummy, w16);
-            ptx::tmem_st16(tS + c * 16, w16);
-          }
-          p_stored = true;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sa[32];
+          ptx::tmem_ld32(tS + c * 32, sa);
+          ptx::tmem_wait_ld_regs(sa);
+          if (diag) mask_chunk(sa, nvis - c * 32);
+#pragma unroll
+          for (int h = 0; h < 16; ++h)
+            mx[h & 3] = ptx::max3(mx[h & 3], __uint_as_float(sa[2 * h]), __uint_as_float(sa[2 * h + 1]));
         }
-        // Apply a pending rescale of O (S_j being complete implies PV_{j-1}
-        // has completed: same issuing thread, in order).  TMEM loads/stores are
-        // warp-collective, so the whole warp takes the branch if any of its
-        // rows needs it (the others scale by 1).
-        if (__any_sync(0xffffffffu, rescale_pending)) {
-          const float alpha = rescale_pending ? alpha_pending : 1.f;
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // log2 domain
+        // The reference moves only when the max grew by more than 2^8 (or on
+        // the first tile), so every p stays below 2^8; moving it rescales O
+        // and l first (S_j complete implies PV_{j-1} complete: same issuing
+        // thread, in order).  TMEM loads/stores are warp-collective, so the
+        // warp rescales if any of its rows needs it (the others scale by 1).
+        const bool move = tmax > m_run + kRescaleThreshold;  // m_run = -inf: any visible key
+        const float alpha = (move && m_run != -INFINITY) ? ptx::ex2(m_run - tmax) : 1.f;
+        if (move) m_run = tmax;
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -535,34 +484,35 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             ptx::tmem_st32(tO + c * 32, o);
           }
-          if (rescale_pending) l_run *= alpha;
-          rescale_pending = false;
+        }
+        l_run *= alpha;
+        // Pass 2 (rolled over pairs of 32-column chunks, the second chunk's
+        // load in flight while the first is converted): P = exp2(S * scale -
+        // m_run) in bf16, each chunk's 16 columns stored straight over S
+        // columns already read.
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+        const uint64_t sc2 = ptx::pack2(sl2, sl2);
+        const uint64_t nm2 = ptx::pack2(-mref, -mref);
+        uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll 1
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t sa[32], sb[32], w16[16];
+          ptx::tmem_ld32(tS + c * 32, sa);
+          ptx::tmem_ld32(tS + (c + 1) * 32, sb);
+          ptx::tmem_wait_ld_regs(sa);
+          if (diag) mask_chunk(sa, nvis - c * 32);
+          exp_chunk_regs(sa, sc2, nm2, rs2, w16);
+          ptx::tmem_st16(tS + c * 16, w16);
+          ptx::tmem_wait_ld_regs(sb);
+          if (diag) mask_chunk(sb, nvis - (c + 1) * 32);
+          exp_chunk_regs(sb, sc2, nm2, rs2, w16);
+          ptx::tmem_st16(tS + (c + 1) * 16, w16);
         }
         {
           const uint64_t r2 = ptx::fadd2(ptx::fadd2(rs2[0], rs2[1]), ptx::fadd2(rs2[2], rs2[3]));
           float rs0, rs1;
           ptx::unpack2(r2, rs0, rs1);
           l_run += rs0 + rs1;
-        }
-        // move the reference when the max grew by more than 2^8: takes effect
-        // for the next tile (O and l are rescaled before its PV)
-        if (j > 0 && tmax > m_run + kRescaleThreshold) {
-          const float mnew = tmax;
-          alpha_pending = ptx::ex2(m_run - mnew);
-          rescale_pending = true;
-          // this tile's P (already relative to the old m_run) joins O before
-          // the rescale, and its sum joins l before the rescale too
-          m_run = mnew;
-        }
-        // P over the first 64 columns of S (bf16 pairs)
-        if (!p_stored) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w16[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) w16[h] = pw[c * 16 + h];
-            ptx::tmem_st16(tS + c * 16, w16);
-          }
         }
         // Cache slots at or past ctx in the last page may hold anything (NaN
         // included) and 0 * NaN is NaN inside PV: zero those V rows before PV
