@@ -171,6 +171,30 @@ def test_large_logit_jumps_rescale_and_redo(cuda_device):
     assert_close(out.cpu(), want, "planted logit jumps")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_every_chunk_kernel_shape(cuda_device, D, G):
+    """Every (head_dim, GQA group) instantiation of the chunk-tile kernel, in a
+    hybrid batch: a chunk with a cached prefix, one without, and decodes."""
+    Hkv = 2
+    Hq = G * Hkv
+    q_lens, seq_lens = [1, 150, 1, 37], [300, 350, 2000, 37]
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=900 + 10 * G + D)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(D)
+    out, wsp = gpu_step(k_cache, v_cache, inp, scale, Hq)
+    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    assert torch.equal(bits(k_cache.cpu()), bits(oc.k))
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    assert_close(out.cpu(), want, f"D {D} G {G}")
+    assert ops.device_status(k_cache, Hq, m.block_table.shape[1], wsp) == 0
+
+
 DECODE_CASES = [
     # (num decodes, ctx range, Hq, Hkv, D) -- decode kernel shapes and fallbacks
     (3, (1, 40), 8, 4, 128),       # fewer pages than workers, ragged pages
