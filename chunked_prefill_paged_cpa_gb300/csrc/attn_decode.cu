@@ -37,6 +37,12 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kPage = 16;
 constexpr float kLazyRescale = 8.0f;  // log2 units
+// Split estimate when part of the grid starts after the chunk kernel: one KV
+// tile of a chunk work item at head_dim 128, the fixed cost of an item (Q
+// load, first tile, epilogue), and the page rate of one decode CTA beside it.
+constexpr double kChunkIterNs = 2200.0;
+constexpr double kChunkItemNs = 12000.0;
+constexpr double kDecodeBytesPerNs = 34.0;
 
 template <int D>
 struct Cfg {
@@ -129,12 +135,38 @@ attn_decode_kernel(const AttnParams p) {
 
   // ---- page-stream offsets of every sequence (exclusive prefix sum) ----
   const int S = p.num_seqs;
+  int c_items = 0, c_ctx = 0;  // chunk work items and longest chunk context (split estimate)
   {
     const int nthr = kWarps * 32;
     const int per = (S + nthr - 1) / nthr;
     const int s0 = threadIdx.x * per, s1 = min(S, s0 + per);
     int local = 0;
-    for (int s = s0; s < s1; ++s) local += seq_decode_pages(p, s) * p.Hkv;
+    for (int s = s0; s < s1; ++s) {
+      local += seq_decode_pages(p, s) * p.Hkv;
+      if (p.decode_early > 0) {
+        const int ql = __ldg(p.query_start_loc + s + 1) - __ldg(p.query_start_loc + s);
+        if (ql > 1) {
+          c_items += p.Hkv * ((ql * G + 255) / 256);
+          c_ctx = max(c_ctx, __ldg(p.seq_lens + s));
+        }
+      }
+    }
+    if (p.decode_early > 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        c_items += __shfl_xor_sync(0xffffffffu, c_items, o);
+        c_ctx = max(c_ctx, __shfl_xor_sync(0xffffffffu, c_ctx, o));
+      }
+      __shared__ int chunk_red[2 * kWarps];
+      if (lane == 0) { chunk_red[warp] = c_items; chunk_red[kWarps + warp] = c_ctx; }
+      __syncthreads();
+      c_items = 0;
+      c_ctx = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        c_items += chunk_red[w];
+        c_ctx = max(c_ctx, chunk_red[kWarps + w]);
+      }
+    }
     // block exclusive scan of `local`
     int incl = local;
 #pragma unroll
@@ -157,14 +189,46 @@ attn_decode_kernel(const AttnParams p) {
   }
   const int64_t N = off[S];
   if (N == 0) return;
-  // At most one worker per page: with W <= N consecutive slice starts
-  // floor(w N / W) strictly increase, so every worker's slice is non-empty and
-  // a segment's contributors are exactly the workers owner(start)..owner(end).
-  const int64_t Wg = (int64_t)gridDim.x * kWarps;
-  const int W = (int)(Wg < N ? Wg : N);
-  const int w = blockIdx.x * kWarps + warp;
-  if (w >= W) return;
-  const int64_t a = (int64_t)w * N / W, b = (int64_t)(w + 1) * N / W;
+  // The page stream [0, N) is [0, NA) for the CTAs that start at once and
+  // [NA, N) for those that start as the chunk kernel's CTAs finish (NA = N
+  // when every CTA starts at once).  Each group splits its range evenly over
+  // its workers, at most one worker per page: with W <= n consecutive slice
+  // starts floor(w n / W) strictly increase, so every slice is non-empty and a
+  // segment's contributors are exactly the workers owner(start)..owner(end),
+  // numbered across both groups (late workers follow the early ones).
+  const int early = p.decode_early > 0 ? min(p.decode_early, (int)gridDim.x) : (int)gridDim.x;
+  const int late = (int)gridDim.x - early;
+  int64_t NA = N;
+  if (late > 0) {
+    // early CTAs stream for T, late ones for T - t_chunk at the same rate:
+    // early * r * T + late * r * (T - t_chunk) = N pages
+    const int64_t rounds = (c_items + p.chunk_grid - 1) / max(p.chunk_grid, 1);
+    const double t_chunk =
+        (double)rounds * (((c_ctx + 127) / 128) * kChunkIterNs * (D / 128.0) + kChunkItemNs);
+    const double r = kDecodeBytesPerNs / (2.0 * kPage * D * 2);  // pages per ns per CTA
+    const double T = ((double)N / r + late * t_chunk) / (double)gridDim.x;
+    NA = (T <= t_chunk) ? N : (int64_t)fmin((double)early * r * T, (double)N);
+  }
+  const int64_t wa = (int64_t)early * kWarps, wb = (int64_t)late * kWarps;
+  const int WA = (int)(wa < NA ? wa : NA), WB = (int)(wb < N - NA ? wb : N - NA);
+  auto owner = [&](int64_t pos) -> int {
+    return pos < NA ? owner_worker(pos, NA, WA) : WA + owner_worker(pos - NA, N - NA, WB);
+  };
+  int w;  // worker index across both groups
+  int64_t a, b;
+  if ((int)blockIdx.x < early) {
+    const int wl = blockIdx.x * kWarps + warp;
+    if (wl >= WA) return;
+    w = wl;
+    a = (int64_t)wl * NA / WA;
+    b = (int64_t)(wl + 1) * NA / WA;
+  } else {
+    const int wl = ((int)blockIdx.x - early) * kWarps + warp;
+    if (wl >= WB) return;
+    w = WA + wl;
+    a = NA + (int64_t)wl * (N - NA) / WB;
+    b = NA + (int64_t)(wl + 1) * (N - NA) / WB;
+  }
 
   if (lane == 0) {
     for (int i = 0; i < NST; ++i) ptx::mbar_init(&bars[i], 1);
@@ -460,8 +524,8 @@ attn_decode_kernel(const AttnParams p) {
         __threadfence();
         __syncwarp();
         const int64_t seg_last = seg_start + cc.n - 1;
-        const int wf = owner_worker(seg_start, N, W);
-        const int wl = owner_worker(seg_last, N, W);
+        const int wf = owner(seg_start);
+        const int wl = owner(seg_last);
         unsigned prev = 0;
         if (lane == 0) prev = atomicAdd(p.counters + sg, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);

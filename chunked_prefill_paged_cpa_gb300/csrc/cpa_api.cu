@@ -61,7 +61,11 @@ static SideStream *side_stream(int device) {
   if (device < 0 || device >= 64) return nullptr;
   SideStream &ss = g_side[device];
   if (!ss.stream) {
-    if (cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) != cudaSuccess ||
+    // highest priority: the chunk kernel's CTAs are dispatched ahead of the
+    // decode CTAs queued behind the SMs the decode kernel starts on
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
+    if (cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
         cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
@@ -209,7 +213,13 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
           cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
         return CPA_ERR_CUDA;
       if (launch_attention_chunk(p, cg, ss->stream) != cudaSuccess) return CPA_ERR_CUDA;
-      if (launch_attention_decode(p, dg, st) != cudaSuccess) return CPA_ERR_CUDA;
+      // the decode kernel takes every SM: dg CTAs start beside the chunk
+      // tiles, the rest as the chunk kernel's CTAs finish
+      AttnParams pd = p;
+      pd.decode_early = dg;
+      pd.chunk_grid = cg;
+      const int gd = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
+      if (launch_attention_decode(pd, gd, st) != cudaSuccess) return CPA_ERR_CUDA;
       if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
           cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
         return CPA_ERR_CUDA;

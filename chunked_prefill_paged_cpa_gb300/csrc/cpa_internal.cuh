@@ -55,6 +55,12 @@ struct AttnParams {
   float scale_log2;          // scale * log2(e): scores live in the log2 domain
   int max_splits;
   int rows_mode;              // row kernel: 0 all tokens, 1 only q_len > 1, 2 only q_len == 1
+  // Streaming decode kernel beside the chunk kernel: its first decode_early
+  // CTAs start at once, the rest as the chunk kernel's chunk_grid CTAs finish.
+  // The page stream is split between the two groups on the device so both end
+  // about together.  0 = every CTA starts at once (even split).
+  int decode_early;
+  int chunk_grid;
   uint32_t *status;
   uint32_t *counters;
   float *part_o;
