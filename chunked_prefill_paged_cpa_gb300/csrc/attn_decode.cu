@@ -530,53 +530,69 @@ attn_decode_kernel(const AttnParams p) {
         if (lane == 0) prev = atomicAdd(p.counters + sg, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == (unsigned)(wl - wf)) {
-          // last contributor: merge every contributor's partial.  The
-          // contributors' (max, sum) pairs are spread over the lanes; each lane
-          // then owns D/32 output dims and streams the partial outputs with
-          // independent loads, 8 contributors at a time.
+          // last contributor: merge every contributor's partial with
+          // log-sum-exp weights, in few dependent rounds of L2 loads (it sits
+          // at the end of this warp's slice).
           __threadfence();
           const int nc = wl - wf + 1;
           const int64_t base = (int64_t)sg + wf;
           __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
                                ((int64_t)tok * p.Hq + (int64_t)cc.g * G) * D;
+          // every row's max over the contributors (lanes stride the contributors)
+          float mx[G];
+#pragma unroll
+          for (int r = 0; r < G; ++r) mx[r] = -INFINITY;
+          for (int c = lane; c < nc; c += 32) {
+#pragma unroll
+            for (int r = 0; r < G; ++r) mx[r] = fmaxf(mx[r], __ldcg(&p.part_ml[(base + c) * G + r].x));
+          }
+#pragma unroll
           for (int r = 0; r < G; ++r) {
-            float mx = -INFINITY;
-            for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(&p.part_ml[(base + c) * G + r].x));
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float lsum = 0.f;
-            for (int c = lane; c < nc; c += 32) {
-              const float2 ml = __ldcg(&p.part_ml[(base + c) * G + r]);
-              lsum += (ml.x == -INFINITY) ? 0.f : ml.y * ptx::ex2(ml.x - mx);
-            }
+            for (int o = 16; o > 0; o >>= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+          }
+          // weighted sums of the partial outputs and row sums: one contributor
+          // per round, all G rows' loads in flight; each lane owns D/32
+          // output dims of every row
+          constexpr int DPL = D / 32;
+          float acc[G][DPL], lsum[G];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-            constexpr int DPL = D / 32;  // dims per lane
-            float acc[DPL];
+          for (int r = 0; r < G; ++r) {
+            lsum[r] = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-            for (int c0 = 0; c0 < nc; c0 += 8) {
-              float wgt[8];
-              float ov[8][DPL];
+            for (int e = 0; e < DPL; ++e) acc[r][e] = 0.f;
+          }
+          for (int c = 0; c < nc; ++c) {
+            const int64_t slot = base + c;
+            float2 ml[G];
+            float ov[G][DPL];
 #pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int c = min(c0 + u, nc - 1);
-                const float mc = __ldcg(&p.part_ml[(base + c) * G + r].x);
-                wgt[u] = (c0 + u < nc && mc != -INFINITY) ? ptx::ex2(mc - mx) : 0.f;
-                const float *src = p.part_o + ((base + c) * G + r) * D + lane * DPL;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) ov[u][e] = __ldcg(src + e);
+            for (int r = 0; r < G; ++r) {
+              ml[r] = __ldcg(&p.part_ml[slot * G + r]);
+              const float *src = p.part_o + (slot * G + r) * D + lane * DPL;
+              if constexpr (DPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                ov[r][0] = v.x; ov[r][1] = v.y; ov[r][2] = v.z; ov[r][3] = v.w;
+              } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                ov[r][0] = v.x; ov[r][1] = v.y;
               }
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[e] = fmaf(ov[u][e], wgt[u], acc[e]);
             }
-            const float inv = 1.f / lsum;
+#pragma unroll
+            for (int r = 0; r < G; ++r) {
+              const float wgt = (ml[r].x != -INFINITY) ? ptx::ex2(ml[r].x - mx[r]) : 0.f;
+              lsum[r] = fmaf(ml[r].y, wgt, lsum[r]);
+#pragma unroll
+              for (int e = 0; e < DPL; ++e) acc[r][e] = fmaf(ov[r][e], wgt, acc[r][e]);
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < G; ++r) {
+            const float inv = 1.f / lsum[r];
 #pragma unroll
             for (int e = 0; e < DPL; e += 2) {
               *reinterpret_cast<__nv_bfloat162 *>(out + r * D + lane * DPL + e) =
-                  __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+                  __floats2bfloat162_rn(acc[r][e] * inv, acc[r][e + 1] * inv);
             }
           }
           if (lane == 0) p.counters[sg] = 0u;
