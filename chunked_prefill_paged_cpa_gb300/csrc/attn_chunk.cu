@@ -12,7 +12,7 @@
 // Each K/V byte read from the paged cache therefore serves all G heads, and
 // the two tiles of a CTA (m = 2mp, 2mp+1) share every K/V tile.
 //
-// Per CTA (320 threads, one CTA per SM):
+// Per CTA (352 threads, one CTA per SM):
 //   warps 0-3  softmax for tile 0, warps 4-7 softmax for tile 1; one thread
 //              per row.  Two short rolled passes over S in TMEM: the tile's
 //              row max (causal mask on diagonal tiles only), then exp2 against
@@ -25,12 +25,15 @@
 //              and of V of kv head g (2-d tensor map over the cache rows);
 //              pages past the sequence are read from an out-of-range row and
 //              arrive as zeros.  K ring of 3 stages, V ring of 2; K runs
-//              one tile ahead of V.
-//   warp 9     allocates the 512 TMEM columns (S0, S1, O0, O1); lane 0 issues
-//              every tcgen05.mma: S_i = Q_i K_j^T (both operands from shared
-//              memory) and O_i += P_i V_j (P from TMEM, V MN-major in shared
-//              memory).  The two tiles ping-pong: while one warpgroup runs its
-//              softmax, the tensor core runs the other tile's PV and next QK^T.
+//              one tile ahead of V.  With the append fused into the call, the
+//              chunk's own pages come from the step's k/v rows instead (tensor
+//              maps over those), chosen once per tile.
+//   warps 9-10 warp 9 allocates the 512 TMEM columns (S0, S1, O0, O1); lane 0
+//              of warp 9 + i issues tile i's tcgen05.mma: S_i = Q_i K_j^T
+//              (both operands from shared memory) and O_i += P_i V_j (P from
+//              TMEM, V MN-major in shared memory).  The two tiles ping-pong:
+//              while one warpgroup runs its softmax, the tensor core runs the
+//              other tile's PV and next QK^T.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -169,7 +172,9 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, int kv_rows) {
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_kin,
+                  const __grid_constant__ CUtensorMap tm_vin, int kv_rows) {
   using C = ChunkCfg<D>;
   constexpr int TM = BM / G;  // tokens per tile
   extern __shared__ unsigned char smem_raw[];
@@ -213,6 +218,10 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
       ptx::prefetch_tmap(&tm_q);
       ptx::prefetch_tmap(&tm_k);
       ptx::prefetch_tmap(&tm_v);
+      if (p.fused) {
+        ptx::prefetch_tmap(&tm_kin);
+        ptx::prefetch_tmap(&tm_vin);
+      }
     }
     uint32_t kvc = 0;  // K/V tiles loaded so far by this CTA
     bool ok = true;
@@ -231,12 +240,52 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
             ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, it.g * G,
                              it.qs + (2 * it.mp + i) * TM, &bs->q_full);
       }
+      // With the append fused in, the chunk's own keys and values are read
+      // from the step's k/v rows: a page made only of new tokens is loaded
+      // from there (encoded below as -2 - its first token).  A page holding
+      // both cached and new rows (a chunk that starts inside a page) is read
+      // from the cache, after this warp has written its new rows there and
+      // fenced them against the bulk-copy proxy; other CTAs may write the same
+      // bytes, with the same values.
+      const int prefix = it.ctx - it.q_len;
+      const int first_new_page = (prefix + kPage - 1) / kPage;  // first page of new tokens only
+      if (p.fused && (prefix % kPage) != 0) {
+        constexpr int CPR = D * 2 / 16;  // 16-byte pieces per row
+        const int nnew = min(it.q_len, first_new_page * kPage - prefix);
+        const int total = nnew * 2 * CPR;
+        const uint4 *kin = static_cast<const uint4 *>(p.k_new);
+        const uint4 *vin = static_cast<const uint4 *>(p.v_new);
+        uint4 *kc4 = static_cast<uint4 *>(const_cast<void *>(p.k_cache));
+        uint4 *vc4 = static_cast<uint4 *>(const_cast<void *>(p.v_cache));
+        const int64_t num_slots = p.num_pages * kPage;
+#pragma unroll
+        for (int u = 0; u < (15 * 2 * CPR + 31) / 32; ++u) {
+          const int c = lane + 32 * u;
+          if (c < total) {
+            const int r = c / (2 * CPR), part = c - r * 2 * CPR;
+            const bool isv = part >= CPR;
+            const int ch = isv ? part - CPR : part;
+            const int64_t t = it.qs + r;
+            const int64_t slot = __ldg(p.slot_mapping + t);
+            const uint4 w = __ldg((isv ? vin : kin) + (t * p.Hkv + it.g) * CPR + ch);
+            if (slot >= num_slots) {
+              atomicOr(p.status, STATUS_BAD_SLOT);
+            } else if (slot >= 0) {
+              const int64_t pg = slot / kPage, off = slot - pg * kPage;
+              (isv ? vc4 : kc4)[((pg * p.Hkv + it.g) * kPage + off) * CPR + ch] = w;
+            }
+          }
+        }
+        ptx::fence_proxy_async_global();
+        __syncwarp();
+      }
       // page ids of the item, 32 at a time in this warp's registers (lane l
       // holds page 32 b + l of block b), the next block prefetched
       const int32_t *bt = p.block_table + (int64_t)it.s * p.max_pages;
       auto load_block = [&](int b) -> int {
         const int pi = 32 * b + lane;
         if (pi >= it.n_pages) return kv_rows;  // past the sequence: zero fill
+        if (p.fused && pi >= first_new_page) return -2 - (it.qs + pi * kPage - prefix);
         const int page = __ldg(bt + pi);
         if (page < 0 || page >= p.num_pages) {
           atomicOr(p.status, STATUS_BAD_PAGE);
@@ -258,19 +307,57 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
         int rows[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, src, (j & 3) * 8 + i);
+        // The source is chosen once per tile: every page from the cache,
+        // every page from the step's rows, or (once per item at most) the
+        // tile where they meet, page by page.  A per-page choice in every
+        // tile made the whole kernel ~30 % slower.
+        const int p0 = 8 * j;
+        const bool some_new = p.fused && max(p0, first_new_page) < min(p0 + 8, it.n_pages);
+        const bool all_new = some_new && p0 >= first_new_page && p0 + 8 <= it.n_pages;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar, C::KV_BYTES);
           if (is_v) {
             // V page-major: one box per page holds all its panels
+            if (!some_new) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              ptx::tma_load_3d(dst + i * C::PAGE_BYTES, &tm_v, 0, rows[i], 0, bar);
+              for (int i = 0; i < 8; ++i)
+                ptx::tma_load_3d(dst + i * C::PAGE_BYTES, &tm_v, 0, rows[i], 0, bar);
+            } else if (all_new) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                ptx::tma_load_4d(dst + i * C::PAGE_BYTES, &tm_vin, 0, -2 - rows[i], 0, it.g, bar);
+            } else {
+              for (int i = 0; i < 8; ++i) {
+                if (rows[i] <= -2)
+                  ptx::tma_load_4d(dst + i * C::PAGE_BYTES, &tm_vin, 0, -2 - rows[i], 0, it.g, bar);
+                else
+                  ptx::tma_load_3d(dst + i * C::PAGE_BYTES, &tm_v, 0, rows[i], 0, bar);
+              }
+            }
           } else {
+            if (!some_new) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+              for (int i = 0; i < 8; ++i)
 #pragma unroll
-              for (int pl = 0; pl < C::PANELS; ++pl)
-                ptx::tma_load_2d(dst + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i], bar);
+                for (int pl = 0; pl < C::PANELS; ++pl)
+                  ptx::tma_load_2d(dst + pl * BN * 128 + i * kPage * 128, &tm_k, pl * 64, rows[i], bar);
+            } else if (all_new) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int pl = 0; pl < C::PANELS; ++pl)
+                  ptx::tma_load_3d(dst + pl * BN * 128 + i * kPage * 128, &tm_kin, pl * 64, it.g,
+                                   -2 - rows[i], bar);
+            } else {
+              for (int i = 0; i < 8; ++i)
+                for (int pl = 0; pl < C::PANELS; ++pl) {
+                  unsigned char *d = dst + pl * BN * 128 + i * kPage * 128;
+                  if (rows[i] <= -2)
+                    ptx::tma_load_3d(d, &tm_kin, pl * 64, it.g, -2 - rows[i], bar);
+                  else
+                    ptx::tma_load_2d(d, &tm_k, pl * 64, rows[i], bar);
+                }
+            }
           }
         }
       };
@@ -646,7 +733,38 @@ cudaError_t launch_dg(const AttnParams &p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_chunk_kernel<D, G><<<grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv, (int)rows);
+  CUtensorMap tkin = tk, tvin = tv;  // unused unless the append is fused
+  if (p.fused) {
+    // the step's new k rows [T][Hkv][D]: box = one 64-dim panel of one kv head
+    // for 16 consecutive tokens, the same [16][64] swizzled layout as a cache page
+    {
+      cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.num_tokens};
+      cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
+      cuuint32_t box[3] = {64, 1, (cuuint32_t)kPage};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (encode(&tkin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.k_new), dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    // the step's new v rows viewed as (64 dims, token, panel, kv head): box =
+    // 16 tokens of one kv head with its panels outermost, as a cache V page
+    {
+      cuuint64_t dims[4] = {64, (cuuint64_t)p.num_tokens, (cuuint64_t)C::PANELS,
+                            (cuuint64_t)p.Hkv};
+      cuuint64_t strides[3] = {(cuuint64_t)p.Hkv * D * 2, 128, (cuuint64_t)D * 2};
+      cuuint32_t box[4] = {64, (cuuint32_t)kPage, (cuuint32_t)C::PANELS, 1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      if (encode(&tvin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(p.v_new), dims,
+                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+  }
+  attn_chunk_kernel<D, G><<<grid, kThreads, C::SMEM, stream>>>(p, tq, tk, tv, tkin, tvin,
+                                                                (int)rows);
   return cudaGetLastError();
 }
 

@@ -28,6 +28,11 @@
 // FMAs and a butterfly reduce-scatter inside each 8-lane group; softmax is
 // online (log2 domain) per group; PV reads the probabilities through a small
 // per-warp shared buffer.
+//
+// Fused append (cpa_append_attention_forward): a second instantiation copies
+// the step's new K/V rows into the cache (the CTAs that start after the chunk
+// kernel, else all of them) and takes each decode's own row from the step's
+// inputs, so no separate append launch has to finish first.
 #include "cpa_internal.cuh"
 #include "ptx.cuh"
 
@@ -110,7 +115,71 @@ __device__ __forceinline__ int owner_worker(int64_t p, int64_t N, int W) {
   return (int)(((p + 1) * (int64_t)W - 1) / N);
 }
 
-template <int D, int G>
+// The step's new K/V rows [T][Hkv][D] copied into their cache slots (the
+// append, when it is fused into the attention call): CTA `cta` of `ncta`
+// takes a grid-stride share, four 16-byte pieces in flight per thread.
+template <int D>
+__device__ __forceinline__ void append_new_rows(const AttnParams &p, int cta, int ncta) {
+  constexpr int CPR = D * 2 / 16;  // 16-byte pieces per row
+  const int64_t total = (int64_t)p.num_tokens * p.Hkv * CPR;
+  const int64_t stride = (int64_t)ncta * blockDim.x;
+  const int64_t num_slots = p.num_pages * kPage;
+  const uint4 *kin = static_cast<const uint4 *>(p.k_new);
+  const uint4 *vin = static_cast<const uint4 *>(p.v_new);
+  uint4 *kc = static_cast<uint4 *>(const_cast<void *>(p.k_cache));
+  uint4 *vc = static_cast<uint4 *>(const_cast<void *>(p.v_cache));
+  for (int64_t i0 = (int64_t)cta * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    uint4 kw[4], vw[4];
+    int64_t sl[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total) {
+        sl[u] = __ldg(p.slot_mapping + i / CPR / p.Hkv);
+        kw[u] = __ldg(kin + i);
+        vw[u] = __ldg(vin + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= total) continue;
+      const int64_t row = i / CPR, t = row / p.Hkv;
+      const int g = (int)(row - t * p.Hkv), ch = (int)(i - row * CPR);
+      if (sl[u] >= num_slots) {
+        if (ch == 0) atomicOr(p.status, STATUS_BAD_SLOT);
+      } else if (sl[u] >= 0) {
+        const int64_t pg = sl[u] / kPage, off = sl[u] - pg * kPage;
+        const int64_t dst = ((pg * p.Hkv + g) * kPage + off) * CPR + ch;
+        kc[dst] = kw[u];
+        vc[dst] = vw[u];
+      }
+    }
+  }
+}
+
+// With the append fused in, a decode's own token (position ctx - 1, in the
+// last page of its segment) may not be in the cache yet when the page is
+// copied in: its K and V rows in the stage are overwritten from the step's
+// k/v rows, one 16-byte piece per lane.  Out of line: inlined, its registers
+// changed how the page loop was allocated and made it ~10 % slower.
+template <int D>
+__device__ __noinline__ void patch_last_row(const AttnParams &p, unsigned char *stage_k,
+                                            int page_bytes, int tok, int g, int ctx, int lane) {
+  constexpr int CPR = D * 2 / 16;
+  const int r = (ctx - 1) & (kPage - 1);
+  if (lane < 2 * CPR) {
+    const bool isv = lane >= CPR;
+    const int ch = isv ? lane - CPR : lane;
+    const uint4 *src = static_cast<const uint4 *>(isv ? p.v_new : p.k_new) +
+                       ((int64_t)tok * p.Hkv + g) * CPR + ch;
+    uint4 *dst = reinterpret_cast<uint4 *>(stage_k + (isv ? page_bytes : 0) + r * D * 2) + ch;
+    *dst = __ldg(src);
+  }
+  __syncwarp();
+}
+
+template <int D, int G, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32, 1)
 attn_decode_kernel(const AttnParams p) {
   using C = Cfg<D>;
@@ -132,6 +201,16 @@ attn_decode_kernel(const AttnParams p) {
   int *valid = reinterpret_cast<int *>(smem + L::FLAGS) + warp * NST;
   float *pbuf = reinterpret_cast<float *>(smem + L::PBUF) + warp * kPage * G;
   int *off = reinterpret_cast<int *>(smem + L::OFFS);
+
+  if constexpr (FUSED) {
+    // The append: every new row into its cache slot, for later steps (this
+    // step's attention takes its own tokens' rows from k_new/v_new).  The
+    // CTAs that start after the chunk kernel do it, or every CTA if none do.
+    const int e0 = p.decode_early > 0 ? min(p.decode_early, (int)gridDim.x) : (int)gridDim.x;
+    const int first = e0 < (int)gridDim.x ? e0 : 0;
+    if ((int)blockIdx.x >= first)
+      append_new_rows<D>(p, (int)blockIdx.x - first, (int)gridDim.x - first);
+  }
 
   // ---- page-stream offsets of every sequence (exclusive prefix sum) ----
   const int S = p.num_seqs;
@@ -294,6 +373,16 @@ attn_decode_kernel(const AttnParams p) {
       ctx = min(__ldg(p.seq_lens + cc.s), p.max_pages * kPage);
       own_start = (cc.pi == 0);
       seg_start = pos - cc.pi;
+      if constexpr (FUSED) {
+        // the decode's own K/V row is patched into the segment's last page
+        // from k_new/v_new: start bringing it into L2
+        constexpr int LPR = D * 2 / 128;  // 128-byte lines per row
+        if (lane < 2 * LPR) {
+          const char *src = static_cast<const char *>(lane < LPR ? p.k_new : p.v_new) +
+                            ((int64_t)tok * p.Hkv + cc.g) * D * 2 + (lane % LPR) * 128;
+          ptx::prefetch_l2(src);
+        }
+      }
       const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(p.q) +
                                ((int64_t)tok * p.Hq + (int64_t)cc.g * G) * D;
 #pragma unroll
@@ -323,6 +412,10 @@ attn_decode_kernel(const AttnParams p) {
       break;
     }
     if (valid[stage]) {
+      if constexpr (FUSED) {
+        if (cc.pi == cc.n - 1)
+          patch_last_row<D>(p, ring + stage * C::STAGE_BYTES, C::PAGE_BYTES, tok, cc.g, ctx, lane);
+      }
       const unsigned char *ks = ring + stage * C::STAGE_BYTES;
       const unsigned char *vs = ks + C::PAGE_BYTES;
       const int key0 = cc.pi * kPage;
@@ -614,19 +707,25 @@ attn_decode_kernel(const AttnParams p) {
   }
 }
 
-template <int D, int G>
-cudaError_t launch_dg(const AttnParams &p, int grid, cudaStream_t stream) {
+template <int D, int G, bool FUSED>
+cudaError_t launch_dgf(const AttnParams &p, int grid, cudaStream_t stream) {
   const size_t smem = Layout<D, G>::bytes(p.num_seqs);
   static bool configured = false;  // per instantiation; attribute is per function
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, G, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Layout<D, G>::bytes(kDecodeMaxSeqs));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  attn_decode_kernel<D, G><<<grid, kWarps * 32, smem, stream>>>(p);
+  attn_decode_kernel<D, G, FUSED><<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const AttnParams &p, int grid, cudaStream_t stream) {
+  return p.fused ? launch_dgf<D, G, true>(p, grid, stream)
+                 : launch_dgf<D, G, false>(p, grid, stream);
 }
 
 }  // namespace

@@ -137,11 +137,21 @@ extern "C" int cpa_kv_append(const void *k, const void *v, const int64_t *slot_m
   return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }
 
-extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cache,
-                                     const int32_t *block_table,
-                                     const int32_t *query_start_loc, const int32_t *seq_lens,
-                                     int32_t num_seqs, float scale, void *out, void *stream,
-                                     const cpa_desc *desc) {
+namespace cpa {
+
+// The step's new rows for a fused append (nullptr k: no append in this call).
+struct NewRows {
+  const void *k = nullptr, *v = nullptr;
+  const int64_t *slots = nullptr;
+};
+
+// Attention over the packed batch; with `nr.k` set the append of the step's
+// new rows is part of the call (fused into the attention kernels where they
+// take the shape, else one append launch ahead of them on the same stream).
+static int attention(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *query_start_loc,
+                     const int32_t *seq_lens, int32_t num_seqs, float scale, void *out,
+                     void *stream, const cpa_desc *desc, const NewRows &nr) {
   int rc = check_shape(desc);
   if (rc != CPA_OK) return rc;
   if (num_seqs < 0) return CPA_ERR_ARG;
@@ -197,6 +207,22 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
     if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
   }
   const bool launch_chunks = tc_chunks && !all_decode;
+  if (nr.k) {
+    if (w.fast_decode && (all_decode || tc_chunks)) {
+      // fused: the chunk and decode kernels read the step's own rows from
+      // k/v; the decode kernel writes every new row into the cache
+      p.fused = 1;
+      p.k_new = nr.k;
+      p.v_new = nr.v;
+      p.slot_mapping = nr.slots;
+    } else {
+      const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
+      if (launch_kv_append(nr.k, nr.v, nr.slots, const_cast<void *>(k_cache),
+                           const_cast<void *>(v_cache), desc->num_tokens, p.Hkv, p.D,
+                           p.page_size, p.num_pages, eb, p.status, st) != cudaSuccess)
+        return CPA_ERR_CUDA;
+    }
+  }
   if (launch_chunks && w.fast_decode) {
     // Both kernels hold one CTA per SM.  When the chunk tiles leave enough
     // SMs free, run them on the side stream while the decodes stream on the
@@ -245,6 +271,38 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
   p.rows_mode = (rows_for_decodes && rows_for_chunks) ? 0 : (rows_for_chunks ? 1 : 2);
   cudaError_t e = launch_attention_rows(p, desc->dtype, st);
   return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+}
+
+}  // namespace cpa
+
+extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_table,
+                                     const int32_t *query_start_loc, const int32_t *seq_lens,
+                                     int32_t num_seqs, float scale, void *out, void *stream,
+                                     const cpa_desc *desc) {
+  return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs, scale,
+                   out, stream, desc, NewRows{});
+}
+
+extern "C" int cpa_append_attention_forward(const void *q, const void *k, const void *v,
+                                            const int64_t *slot_mapping, void *k_cache,
+                                            void *v_cache, const int32_t *block_table,
+                                            const int32_t *query_start_loc,
+                                            const int32_t *seq_lens, int32_t num_seqs,
+                                            float scale, void *out, void *stream,
+                                            const cpa_desc *desc) {
+  int rc = check_shape(desc);
+  if (rc != CPA_OK) return rc;
+  if (num_seqs < 0) return CPA_ERR_ARG;
+  if (num_seqs == 0 || desc->num_tokens == 0) return CPA_OK;
+  if (!k || !v || !slot_mapping) return CPA_ERR_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8)) return CPA_ERR_ARG;
+  NewRows nr;
+  nr.k = k;
+  nr.v = v;
+  nr.slots = slot_mapping;
+  return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs, scale,
+                   out, stream, desc, nr);
 }
 
 extern "C" int cpa_read_device_status(const cpa_desc *desc, void *stream, int32_t *status_out) {

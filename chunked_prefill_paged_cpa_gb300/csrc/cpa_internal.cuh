@@ -61,6 +61,15 @@ struct AttnParams {
   // about together.  0 = every CTA starts at once (even split).
   int decode_early;
   int chunk_grid;
+  // Fused append (cpa_append_attention_forward): the step's new k/v rows
+  // [num_tokens][Hkv][D] and their cache slots.  The attention kernels take
+  // the step's own keys and values from k_new/v_new and the decode kernel also
+  // writes every new row into the cache.  fused = 0: the cache already holds
+  // them (cpa_kv_append ran first).
+  int fused;
+  const void *k_new;
+  const void *v_new;
+  const int64_t *slot_mapping;
   uint32_t *status;
   uint32_t *counters;
   float *part_o;

@@ -73,6 +73,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.cpa_kv_append.restype = ctypes.c_int
         lib.cpa_attention_forward.argtypes = [P, P, P, P, P, P, I32, F, P, P, D]
         lib.cpa_attention_forward.restype = ctypes.c_int
+        lib.cpa_append_attention_forward.argtypes = [P, P, P, P, P, P, P, P, P, I32, F, P, P, D]
+        lib.cpa_append_attention_forward.restype = ctypes.c_int
         lib.cpa_attention_forward_noalloc.argtypes = [P, P, P, P, P, P, I32, F, P, P, D]
         lib.cpa_attention_forward_noalloc.restype = ctypes.c_int
         lib.cpa_read_device_status.argtypes = [D, P, ctypes.POINTER(I32)]
@@ -101,6 +103,15 @@ def cpa_attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq
     return int(load().cpa_attention_forward(q, k_cache, v_cache, block_table,
                                             query_start_loc, seq_lens, int(num_seqs),
                                             float(scale), out, stream, ctypes.byref(desc)))
+
+
+def cpa_append_attention_forward(q, k, v, slot_mapping, k_cache, v_cache, block_table,
+                                 query_start_loc, seq_lens, num_seqs, scale, out, stream,
+                                 desc: CpaDesc) -> int:
+    return int(load().cpa_append_attention_forward(q, k, v, slot_mapping, k_cache, v_cache,
+                                                   block_table, query_start_loc, seq_lens,
+                                                   int(num_seqs), float(scale), out, stream,
+                                                   ctypes.byref(desc)))
 
 
 def cpa_attention_forward_noalloc(q, k_cache, v_cache, block_table, query_start_loc,
@@ -184,6 +195,23 @@ def attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq_len
                                scale, _ptr(out), _stream(stream), desc)
     if rc != CPA_OK:
         raise CpaError(rc, "cpa_attention_forward")
+    return out
+
+
+def append_attention_forward(q, k, v, slot_mapping, k_cache, v_cache, block_table,
+                             query_start_loc, seq_lens, scale, workspace, out=None,
+                             stream=None) -> torch.Tensor:
+    """kv_append followed by attention_forward, as one C-ABI call (the append
+    fused into the attention kernels where they take the shape)."""
+    if out is None:
+        out = torch.empty_like(q)
+    desc = make_desc(k_cache, q.shape[1], q.shape[0], block_table.shape[1], workspace)
+    rc = cpa_append_attention_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),
+                                      _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                      _ptr(query_start_loc), _ptr(seq_lens), seq_lens.shape[0],
+                                      scale, _ptr(out), _stream(stream), desc)
+    if rc != CPA_OK:
+        raise CpaError(rc, "cpa_append_attention_forward")
     return out
 
 

@@ -115,6 +115,34 @@ int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cach
                           int32_t num_seqs, float scale, void *out, void *stream,
                           const cpa_desc *desc);
 
+/* KV append and attention forward of one step in one call: the same results
+ * as cpa_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream)
+ * followed by cpa_attention_forward(...) on the same stream -- the cache holds
+ * the same bytes afterwards and out the same values -- without the separate
+ * append launch ("Chunked Prefill on an M5 Max", section "Wiring it into the
+ * loop": appending is part of each chunk's fixed cost).
+ *  - Arguments: those of the two calls; k, v [num_tokens][Hkv][D] in the
+ *    cache dtype and 16-byte aligned, slot_mapping int64 [num_tokens] and
+ *    8-byte aligned.  slot_mapping[t] must be the cache slot of token t's
+ *    position in its sequence (block_table[s][pos / 16] * 16 + pos % 16);
+ *    tokens with a negative slot are not written, and no query may attend to
+ *    them.
+ *  - Where the bf16 attention kernels take the shape (head_dim 64 or 128,
+ *    GQA group 2, 4 or 8 with group * head_dim <= 512), the append is fused
+ *    into them: the step's own keys and values are read from k/v, not from the
+ *    cache, and the decode kernel writes every new row into its slot.  In
+ *    that case each sequence may appear only once in the batch, and the cache
+ *    rows this call writes are complete only when the call's work on `stream`
+ *    has finished.  Otherwise the call launches the append and then the
+ *    attention on `stream`.
+ *  - Errors: those of the two calls; slots >= num_pages * page_size raise the
+ *    device status word and are not written. */
+int cpa_append_attention_forward(const void *q, const void *k, const void *v,
+                                 const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 const int32_t *block_table, const int32_t *query_start_loc,
+                                 const int32_t *seq_lens, int32_t num_seqs, float scale,
+                                 void *out, void *stream, const cpa_desc *desc);
+
 /* Size of the scratch array built into the library for
  * cpa_attention_forward_noalloc: 16 MiB of device memory on every GPU that
  * loads the library, held until the process exits. */

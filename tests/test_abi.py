@@ -74,6 +74,27 @@ def test_bad_descriptor_rejected_before_launch(lib, field, value, code):
     P = ctypes.c_void_p(256)
     assert ops.cpa_kv_append(P, P, P, P, P, d, None) == code
     assert ops.cpa_attention_forward(P, P, P, P, P, P, 2, 0.1, P, None, d) == code
+    assert ops.cpa_append_attention_forward(P, P, P, P, P, P, P, P, P, 2, 0.1, P, None, d) == code
+
+
+def test_fused_append_call_validates_both_halves(lib):
+    d = _desc()
+    P = ctypes.c_void_p(4096)
+    fa = ops.cpa_append_attention_forward
+    # the append's arguments
+    assert fa(P, None, P, P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, P, None, P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, P, P, None, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, ctypes.c_void_p(4100), P, P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, P, P, ctypes.c_void_p(4100), P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    # the attention's arguments
+    assert fa(P, P, P, P, P, P, None, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, P, P, P, P, P, P, P, P, 2, 0.1, P, None, d) == ops.CPA_ERR_WORKSPACE
+    d.workspace, d.workspace_bytes = 4096, 1 << 30
+    assert fa(P, P, P, P, P, P, P, P, P, 2, -1.0, P, None, d) == ops.CPA_ERR_ARG
+    assert fa(P, P, P, P, P, P, P, P, P, 11, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    # empty step
+    assert fa(P, P, P, P, P, P, P, P, P, 0, 0.1, P, None, _desc(num_tokens=0)) == ops.CPA_OK
 
 
 def test_null_and_misaligned_pointers_rejected(lib):

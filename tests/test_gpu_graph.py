@@ -69,3 +69,50 @@ def test_captured_step_replays_bit_for_bit(cuda_device):
         assert torch.equal(bits(vg), bits(vc)), f"replay {replay}: V cache"
         assert torch.equal(bits(out_g), bits(out_e)), f"replay {replay}: attention output"
     assert ops.device_status(kg, Hq, max_pages, ws_g) == 0
+
+
+def test_captured_fused_call_replays_bit_for_bit(cuda_device):
+    """cpa_append_attention_forward (the append fused into the attention
+    kernels) captured in a CUDA graph: every replay leaves the same cache bytes
+    and output bits as the eager call."""
+    q_lens = [33, 1, 129, 1, 1, 1]
+    seq_lens = [50, 1100, 429, 3, 700, 2000]
+    Hq, Hkv, D = 32, 8, 128
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=322)
+    dev = cuda_device
+    m = st["meta"].to(dev)
+    q, k, v = st["q"].to(dev), st["k_new"].to(dev), st["v_new"].to(dev)
+    k0, v0 = st["oracle_cache"].k.to(dev), st["oracle_cache"].v.to(dev)
+    scale = 1 / math.sqrt(D)
+    max_pages = m.block_table.shape[1]
+
+    kc, vc = k0.clone(), v0.clone()
+    ws_e = ops.workspace_for(kc, Hq, max_pages, m.num_seqs)
+    out_e = ops.append_attention_forward(q, k, v, m.slot_mapping, kc, vc, m.block_table,
+                                         m.query_start_loc, m.seq_lens, scale, ws_e)
+    torch.cuda.synchronize()
+
+    kg, vg = k0.clone(), v0.clone()
+    ws_g = ops.workspace_for(kg, Hq, max_pages, m.num_seqs)
+    out_g = torch.empty_like(out_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        ops.append_attention_forward(q, k, v, m.slot_mapping, kg, vg, m.block_table,
+                                     m.query_start_loc, m.seq_lens, scale, ws_g, out=out_g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ops.append_attention_forward(q, k, v, m.slot_mapping, kg, vg, m.block_table,
+                                     m.query_start_loc, m.seq_lens, scale, ws_g, out=out_g)
+    for replay in range(2):
+        kg.copy_(k0)
+        vg.copy_(v0)
+        out_g.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(bits(kg), bits(kc)), f"replay {replay}: K cache"
+        assert torch.equal(bits(vg), bits(vc)), f"replay {replay}: V cache"
+        assert torch.equal(bits(out_g), bits(out_e)), f"replay {replay}: attention output"
+    assert ops.device_status(kg, Hq, max_pages, ws_g) == 0

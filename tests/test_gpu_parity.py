@@ -350,12 +350,19 @@ def oracle_rows_for_seq(ws, rid, seq_len, q_len, rows):
     return oracle.attention(q, kc, vc, bt, qsl, sl, sh.scale, rows=rows)
 
 
-def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24):
+def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24, fused=False):
     sc = workloads.scenario(name)
     ws = workloads.WorkloadState(sc, device=cuda_device)
     inp = ws.step(0)
     m = inp["meta"]
-    out, _ = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, sc.shape.num_q_heads)
+    if fused:
+        wsp = ops.workspace_for(ws.k_cache, sc.shape.num_q_heads, m.block_table.shape[1],
+                                m.num_seqs)
+        out = ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping,
+                                           ws.k_cache, ws.v_cache, m.block_table,
+                                           m.query_start_loc, m.seq_lens, sc.shape.scale, wsp)
+    else:
+        out, _ = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, sc.shape.num_q_heads)
     torch.cuda.synchronize()
     # paging bit-exact: the package's slots equal the oracle's, and the cache
     # holds the new rows at exactly those slots
