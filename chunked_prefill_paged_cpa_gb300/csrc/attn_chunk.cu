@@ -144,6 +144,23 @@ __device__ bool warp_find_item(const AttnParams &p, int item, Item &it) {
   return true;
 }
 
+// The work items of one CTA, wave by wave: item w*grid + b in even waves and
+// (w+1)*grid - 1 - b in odd ones.  Items come longest first (later query tiles
+// see more keys), so a CTA whose first item is long gets a short second one;
+// plain round-robin gave the CTA with the longest item the longest of the
+// second wave too.  Every warp of the CTA walks the same sequence.
+struct ItemSeq {
+  int b, grid, total, w;
+  __device__ int next() {
+    for (;;) {
+      const int wv = w++;
+      if ((int64_t)wv * grid >= total) return total;
+      const int it = (wv & 1) ? (wv + 1) * grid - 1 - b : wv * grid + b;
+      if (it < total) return it;
+    }
+  }
+};
+
 // Keys at positions >= n of a 32-column chunk become -inf.
 __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
 #pragma unroll
@@ -226,7 +243,8 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     uint32_t kvc = 0;  // K/V tiles loaded so far by this CTA
     bool ok = true;
     int n = 0;
-    for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
+    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    for (int item = seq.next(); ok && item < total; item = seq.next(), ++n) {
       Item it;
       if (!warp_find_item<G>(p, item, it)) break;
       // the Q buffers are free once every MMA of the previous item completed
@@ -434,7 +452,8 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     uint32_t pcnt = 0;  // P tiles of this slot consumed
     bool ok = true;
     int n = 0;
-    for (int item = blockIdx.x; ok && item < total; item += gridDim.x, ++n) {
+    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    for (int item = seq.next(); ok && item < total; item = seq.next(), ++n) {
       Item it;
       if (!warp_find_item<G>(p, item, it)) break;
       if (lane == 0) {
@@ -523,7 +542,8 @@ attn_chunk_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_q,
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, ocnt = 0, kvb = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+    ItemSeq seq{(int)blockIdx.x, (int)gridDim.x, total, 0};
+    for (int item = seq.next(); ok && item < total; item = seq.next()) {
       Item it;
       if (!warp_find_item<G>(p, item, it)) break;
       const int n_mine = ti ? it.n_kv1 : it.n_kv0;
