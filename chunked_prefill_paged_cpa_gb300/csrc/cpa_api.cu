@@ -224,14 +224,17 @@ static int attention(const void *q, const void *k_cache, const void *v_cache,
     }
   }
   if (launch_chunks && w.fast_decode) {
-    // Both kernels hold one CTA per SM.  When the chunk tiles leave enough
-    // SMs free, run them on the side stream while the decodes stream on the
-    // caller's stream over the remaining SMs; otherwise run them one after
-    // the other on the caller's stream.
+    // Both kernels hold one CTA per SM.  The chunk tiles run on the side
+    // stream (highest priority, so their CTAs are placed first) and the
+    // decode kernel on the caller's stream takes every SM: dg CTAs start
+    // beside the chunk tiles, the rest as the chunk kernel's CTAs finish
+    // (with dg = 0 all of them, the page stream split evenly).  When the chunk
+    // items outnumber the SMs, the CTAs left with one item finish a wave
+    // early and the decodes run there.
     const int cg = chunk_grid_estimate(p, sms);
     int dg = sms - cg;
     if (dg > kDecodeMaxWorkers / 8) dg = kDecodeMaxWorkers / 8;
-    if (dg >= sms / 8) {
+    {
       std::lock_guard<std::mutex> lock(g_side_mutex);
       SideStream *ss = side_stream(dev);
       if (!ss) return CPA_ERR_CUDA;
@@ -239,8 +242,6 @@ static int attention(const void *q, const void *k_cache, const void *v_cache,
           cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
         return CPA_ERR_CUDA;
       if (launch_attention_chunk(p, cg, ss->stream) != cudaSuccess) return CPA_ERR_CUDA;
-      // the decode kernel takes every SM: dg CTAs start beside the chunk
-      // tiles, the rest as the chunk kernel's CTAs finish
       AttnParams pd = p;
       pd.decode_early = dg;
       pd.chunk_grid = cg;
@@ -249,10 +250,6 @@ static int attention(const void *q, const void *k_cache, const void *v_cache,
       if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
           cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
         return CPA_ERR_CUDA;
-    } else {
-      if (launch_attention_chunk(p, cg, st) != cudaSuccess) return CPA_ERR_CUDA;
-      int g2 = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
-      if (launch_attention_decode(p, g2, st) != cudaSuccess) return CPA_ERR_CUDA;
     }
     rows_for_decodes = rows_for_chunks = false;
   } else {
