@@ -158,21 +158,95 @@ __device__ __forceinline__ void append_new_rows(const AttnParams &p, int cta, in
   }
 }
 
+// The last contributor of a (sequence, kv head) merges the nc partials in
+// slots base .. base+nc-1 with log-sum-exp weights: one pass for every row's
+// maximum (lanes stride the contributors), then U contributors per round with
+// every row's (max, sum) and each lane's slice of every row's output in
+// flight; each lane owns D/32 output dims of every row.  Out of line: a
+// segment in a region of short slices has tens of contributors, and with the
+// merge inlined, more loads in flight changed how the page loop was allocated.
+template <int D, int G>
+__device__ __noinline__ void merge_partials(const float *part_o, const float2 *part_ml,
+                                            int64_t base, int nc, __nv_bfloat16 *out, int lane) {
+  constexpr int DPL = D / 32;
+  constexpr int U = 4;
+  float mx[G];
+#pragma unroll
+  for (int r = 0; r < G; ++r) mx[r] = -INFINITY;
+  for (int c = lane; c < nc; c += 32) {
+#pragma unroll
+    for (int r = 0; r < G; ++r) mx[r] = fmaxf(mx[r], __ldcg(&part_ml[(base + c) * G + r].x));
+  }
+#pragma unroll
+  for (int r = 0; r < G; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+  }
+  float acc[G][DPL], lsum[G];
+#pragma unroll
+  for (int r = 0; r < G; ++r) {
+    lsum[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[r][e] = 0.f;
+  }
+  for (int c0 = 0; c0 < nc; c0 += U) {
+    float2 ml[U][G];
+    float ov[U][G][DPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t slot = base + min(c0 + u, nc - 1);
+#pragma unroll
+      for (int r = 0; r < G; ++r) {
+        ml[u][r] = __ldcg(&part_ml[slot * G + r]);
+        const float *src = part_o + (slot * G + r) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+          ov[u][r][0] = v.x; ov[u][r][1] = v.y; ov[u][r][2] = v.z; ov[u][r][3] = v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+          ov[u][r][0] = v.x; ov[u][r][1] = v.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int r = 0; r < G; ++r) {
+        const float wgt = (c0 + u < nc && ml[u][r].x != -INFINITY)
+                              ? ptx::ex2(ml[u][r].x - mx[r]) : 0.f;
+        lsum[r] = fmaf(ml[u][r].y, wgt, lsum[r]);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[r][e] = fmaf(ov[u][r][e], wgt, acc[r][e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < G; ++r) {
+    const float inv = 1.f / lsum[r];
+#pragma unroll
+    for (int e = 0; e < DPL; e += 2) {
+      *reinterpret_cast<__nv_bfloat162 *>(out + r * D + lane * DPL + e) =
+          __floats2bfloat162_rn(acc[r][e] * inv, acc[r][e + 1] * inv);
+    }
+  }
+}
+
 // With the append fused in, a decode's own token (position ctx - 1, in the
 // last page of its segment) may not be in the cache yet when the page is
 // copied in: its K and V rows in the stage are overwritten from the step's
 // k/v rows, one 16-byte piece per lane.  Out of line: inlined, its registers
 // changed how the page loop was allocated and made it ~10 % slower.
 template <int D>
-__device__ __noinline__ void patch_last_row(const AttnParams &p, unsigned char *stage_k,
-                                            int page_bytes, int tok, int g, int ctx, int lane) {
+__device__ __noinline__ void patch_last_row(const void *k_new, const void *v_new, int Hkv,
+                                            unsigned char *stage_k, int page_bytes, int tok,
+                                            int g, int ctx, int lane) {
   constexpr int CPR = D * 2 / 16;
   const int r = (ctx - 1) & (kPage - 1);
   if (lane < 2 * CPR) {
     const bool isv = lane >= CPR;
     const int ch = isv ? lane - CPR : lane;
-    const uint4 *src = static_cast<const uint4 *>(isv ? p.v_new : p.k_new) +
-                       ((int64_t)tok * p.Hkv + g) * CPR + ch;
+    const uint4 *src = static_cast<const uint4 *>(isv ? v_new : k_new) +
+                       ((int64_t)tok * Hkv + g) * CPR + ch;
     uint4 *dst = reinterpret_cast<uint4 *>(stage_k + (isv ? page_bytes : 0) + r * D * 2) + ch;
     *dst = __ldg(src);
   }
@@ -414,7 +488,8 @@ attn_decode_kernel(const AttnParams p) {
     if (valid[stage]) {
       if constexpr (FUSED) {
         if (cc.pi == cc.n - 1)
-          patch_last_row<D>(p, ring + stage * C::STAGE_BYTES, C::PAGE_BYTES, tok, cc.g, ctx, lane);
+          patch_last_row<D>(p.k_new, p.v_new, p.Hkv, ring + stage * C::STAGE_BYTES,
+                            C::PAGE_BYTES, tok, cc.g, ctx, lane);
       }
       const unsigned char *ks = ring + stage * C::STAGE_BYTES;
       const unsigned char *vs = ks + C::PAGE_BYTES;
@@ -623,71 +698,12 @@ attn_decode_kernel(const AttnParams p) {
         if (lane == 0) prev = atomicAdd(p.counters + sg, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
         if (prev == (unsigned)(wl - wf)) {
-          // last contributor: merge every contributor's partial with
-          // log-sum-exp weights, in few dependent rounds of L2 loads (it sits
-          // at the end of this warp's slice).
+          // last contributor: merge every contributor's partial
           __threadfence();
-          const int nc = wl - wf + 1;
-          const int64_t base = (int64_t)sg + wf;
-          __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) +
-                               ((int64_t)tok * p.Hq + (int64_t)cc.g * G) * D;
-          // every row's max over the contributors (lanes stride the contributors)
-          float mx[G];
-#pragma unroll
-          for (int r = 0; r < G; ++r) mx[r] = -INFINITY;
-          for (int c = lane; c < nc; c += 32) {
-#pragma unroll
-            for (int r = 0; r < G; ++r) mx[r] = fmaxf(mx[r], __ldcg(&p.part_ml[(base + c) * G + r].x));
-          }
-#pragma unroll
-          for (int r = 0; r < G; ++r) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
-          }
-          // weighted sums of the partial outputs and row sums: one contributor
-          // per round, all G rows' loads in flight; each lane owns D/32
-          // output dims of every row
-          constexpr int DPL = D / 32;
-          float acc[G][DPL], lsum[G];
-#pragma unroll
-          for (int r = 0; r < G; ++r) {
-            lsum[r] = 0.f;
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[r][e] = 0.f;
-          }
-          for (int c = 0; c < nc; ++c) {
-            const int64_t slot = base + c;
-            float2 ml[G];
-            float ov[G][DPL];
-#pragma unroll
-            for (int r = 0; r < G; ++r) {
-              ml[r] = __ldcg(&p.part_ml[slot * G + r]);
-              const float *src = p.part_o + (slot * G + r) * D + lane * DPL;
-              if constexpr (DPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                ov[r][0] = v.x; ov[r][1] = v.y; ov[r][2] = v.z; ov[r][3] = v.w;
-              } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                ov[r][0] = v.x; ov[r][1] = v.y;
-              }
-            }
-#pragma unroll
-            for (int r = 0; r < G; ++r) {
-              const float wgt = (ml[r].x != -INFINITY) ? ptx::ex2(ml[r].x - mx[r]) : 0.f;
-              lsum[r] = fmaf(ml[r].y, wgt, lsum[r]);
-#pragma unroll
-              for (int e = 0; e < DPL; ++e) acc[r][e] = fmaf(ov[r][e], wgt, acc[r][e]);
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < G; ++r) {
-            const float inv = 1.f / lsum[r];
-#pragma unroll
-            for (int e = 0; e < DPL; e += 2) {
-              *reinterpret_cast<__nv_bfloat162 *>(out + r * D + lane * DPL + e) =
-                  __floats2bfloat162_rn(acc[r][e] * inv, acc[r][e + 1] * inv);
-            }
-          }
+          merge_partials<D, G>(p.part_o, p.part_ml, (int64_t)sg + wf, wl - wf + 1,
+                               static_cast<__nv_bfloat16 *>(p.out) +
+                                   ((int64_t)tok * p.Hq + (int64_t)cc.g * G) * D,
+                               lane);
           if (lane == 0) p.counters[sg] = 0u;
         }
       }
