@@ -356,11 +356,15 @@ attn_decode_kernel(const AttnParams p) {
     // early CTAs stream for T, late ones for T - t_chunk at the same rate:
     // early * r * T + late * r * (T - t_chunk) = N pages
     const int64_t rounds = (c_items + p.chunk_grid - 1) / max(p.chunk_grid, 1);
-    const double t_chunk =
-        (double)rounds * (((c_ctx + 127) / 128) * kChunkIterNs * (D / 128.0) + kChunkItemNs);
-    const double r = kDecodeBytesPerNs / (2.0 * kPage * D * 2);  // pages per ns per CTA
-    const double T = ((double)N / r + late * t_chunk) / (double)gridDim.x;
-    NA = (T <= t_chunk) ? N : (int64_t)fmin((double)early * r * T, (double)N);
+    // single precision: the split only has to be close, and every thread
+    // computes the same value (fp64 is slow on this part)
+    const float t_chunk = (float)rounds * ((float)((c_ctx + 127) / 128) *
+                                           (float)(kChunkIterNs * (D / 128.0)) +
+                                           (float)kChunkItemNs);
+    constexpr float r = (float)(kDecodeBytesPerNs / (2.0 * kPage * D * 2));  // pages/ns/CTA
+    const float T = ((float)N * (1.f / r) + (float)late * t_chunk) / (float)gridDim.x;
+    NA = (T <= t_chunk) ? N : (int64_t)fminf((float)early * r * T, (float)N);
+    if (NA > N) NA = N;
   }
   const int64_t wa = (int64_t)early * kWarps, wb = (int64_t)late * kWarps;
   const int WA = (int)(wa < NA ? wa : NA), WB = (int)(wb < N - NA ? wb : N - NA);
