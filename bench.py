@@ -469,60 +469,135 @@ def run_gpu(args, world, rank, local):
         cb = cpu_oracle_time(sc, ws, inp, initial, budget_s=args.ref_budget)
         cb.pop("seconds", None)
         line["cpu_baseline"] = cb
+    if world == 1 and not args.no_extras:
+        # every configuration, timed the same way in the same run, and the
+        # budget sweep with its free-ride grid (single-GPU runs only)
+        del ws, inp, initial, wsp, out, dbuf, dmeta, dbuf2, dmeta2, outs2
+        torch.cuda.empty_cache()
+        line["workloads"] = measure_workloads(
+            ["page1_default", "large_budget", "long_context", "decode_only", "oneshot_8192",
+             "tiny"], dev, flush, stream, peaks, args.steps, args.warmup, args.seed)
+        line["sweep"] = measure_sweep(dev, flush, stream, peaks, args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
 
-def run_sweep(args):
+def _time_calls(fn, flush, stream, n):
+    """Device time of n calls of fn, each after an L2 flush (CUDA events on
+    the launching stream); returns a list of microseconds."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 for a, b in ev]
+
+
+def _fused_call(ws, inp, stream):
+    """One step (append + attention) through cpa_append_attention_forward;
+    repeating it is idempotent (the append writes the same bytes)."""
+    from chunked_prefill_paged_cpa_gb300 import ops
+    sh = ws.sc.shape
+    m = inp["meta"]
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs)
+    out = torch.empty_like(inp["q"])
+
+    def call():
+        ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping, ws.k_cache,
+                                     ws.v_cache, m.block_table, m.query_start_loc, m.seq_lens,
+                                     sh.scale, wsp, out=out, stream=stream)
+    return call
+
+
+def _roofline_entry(m, sh, us, peaks):
+    eb = torch.empty((), dtype=sh.dtype).element_size()
+    c = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, eb)
+    t_b = c["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_f = c["flops"] / (peaks["bf16_tflops"] * 1e12)
+    return c, {"roofline_us": max(t_b, t_f) * 1e6, "frac": max(t_b, t_f) * 1e6 / us,
+               "bound": "hbm" if t_b >= t_f else "tensor",
+               "t_hbm_us": t_b * 1e6, "t_tensor_us": t_f * 1e6}
+
+
+def measure_workloads(names, dev, flush, stream, peaks, steps, warmup, seed):
+    """Every named workload's first step through the fused call, timed like the
+    headline (L2 flushed before each call, CUDA events on the launching
+    stream): step time, query tokens/s and the fraction of the step roofline;
+    decode-only steps also report achieved HBM bandwidth."""
+    from chunked_prefill_paged_cpa_gb300 import workloads
+    res = {}
+    for name in names:
+        sc = workloads.scenario(name, seed)
+        ws = workloads.WorkloadState(sc, device=dev)
+        inp = ws.step(0)
+        m = inp["meta"]
+        sh = sc.shape
+        call = _fused_call(ws, inp, stream)
+        for _ in range(warmup):
+            flush.fill_(1)
+            call()
+        us = _time_calls(call, flush, stream, steps)
+        mean = sum(us) / len(us)
+        c, roof = _roofline_entry(m, sh, mean, peaks)
+        e = {"step_us": mean, "step_us_min": min(us), "tokens_per_s": m.num_tokens / (mean * 1e-6),
+             "query_tokens": m.num_tokens, "num_seqs": m.num_seqs,
+             "kv_tokens": int(sum(m.seq_lens_list)),
+             "dtype": "bf16" if sh.dtype == torch.bfloat16 else "f32"}
+        if sh.dtype == torch.bfloat16:
+            e["step_roofline"] = roof
+        else:
+            e["step_roofline"] = None
+            e["note"] = "fp32 parity configuration: launch latency only"
+        if all(q == 1 for q in m.q_lens):
+            gbs = (c["bytes"] + c["append_bytes"] // 2) / (mean * 1e-6) / 1e9
+            e["hbm"] = {"achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
+                        "frac": gbs / peaks["hbm_gbs"],
+                        "bytes": c["bytes"] + c["append_bytes"] // 2}
+        res[name] = e
+        del ws, inp, call
+        torch.cuda.empty_cache()
+    return res
+
+
+def measure_sweep(dev, flush, stream, peaks, seed, budgets=(256, 512, 2048, 16384),
+                  free_ride_grid=tuple(range(0, 2049, 64)), free_ride_steps=8):
     """Budget sweep: an 8192-token prompt prefilled from scratch beside 32
     decodes, once per token budget, every step timed (append + attention, L2
     flushed before each); per budget the mean step time, the prompt's total
-    prefill time and the mean fraction of each step's roofline."""
+    prefill time and the mean fraction of each step's roofline.  Then the
+    free ride: the default step's 32 decodes beside a chunk of C tokens at
+    offset 3840, C on a grid from 0 (decodes alone); the largest C whose step
+    stays within 5 % of the decodes-alone step, beside the attention form of
+    the pages' estimate (the chunk's FLOPs at bf16 peak fit in the time the
+    decodes' KV bytes take at HBM peak)."""
     from chunked_prefill_paged_cpa_gb300 import ops, workloads
-    dev = torch.device("cuda:0")
-    torch.cuda.set_device(dev)
-    ops.load()
-    peaks, peak_src = load_peaks()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
     rows = []
-    for budget in (256, 512, 2048, 16384):
-        sc = workloads.budget_sweep(budget, args.seed)
+    for budget in budgets:
+        sc = workloads.budget_sweep(budget, seed)
         ws = workloads.WorkloadState(sc, device=dev)
         sh = sc.shape
-        eb = torch.empty((), dtype=sh.dtype).element_size()
         steps = [ws.step(k) for k in range(len(sc.plans))]
-        max_pages = max(s["meta"].block_table.shape[1] for s in steps)
-        max_seqs = max(s["meta"].num_seqs for s in steps)
+        max_pages = max(x["meta"].block_table.shape[1] for x in steps)
+        max_seqs = max(x["meta"].num_seqs for x in steps)
         wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, max_pages, max_seqs)
-        outs = [torch.empty_like(s["q"]) for s in steps]
+        outs = [torch.empty_like(x["q"]) for x in steps]
 
         def one(k):
-            s, m = steps[k], steps[k]["meta"]
-            ops.append_attention_forward(s["q"], s["k"], s["v"], m.slot_mapping, ws.k_cache,
+            x, m = steps[k], steps[k]["meta"]
+            ops.append_attention_forward(x["q"], x["k"], x["v"], m.slot_mapping, ws.k_cache,
                                          ws.v_cache, m.block_table, m.query_start_loc,
                                          m.seq_lens, sh.scale, wsp, out=outs[k], stream=stream)
 
         for k in range(len(steps)):       # warm-up pass (appends are idempotent)
             one(k)
         torch.cuda.synchronize()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in steps]
+        us = []
         for k in range(len(steps)):
-            flush.fill_(k & 0xff)
-            ev[k][0].record(stream)
-            one(k)
-            ev[k][1].record(stream)
-        torch.cuda.synchronize()
-        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
-        fr = []
-        for k, s in enumerate(steps):
-            m = s["meta"]
-            c = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads,
-                            sh.head_dim, eb)
-            roof = max(c["bytes"] / (peaks["hbm_gbs"] * 1e9), c["flops"] / (peaks["bf16_tflops"] * 1e12))
-            fr.append(roof * 1e6 / us[k])
+            us += _time_calls(lambda: one(k), flush, stream, 1)
+        fr = [_roofline_entry(x["meta"], sh, us[k], peaks)[1]["frac"] for k, x in enumerate(steps)]
         rows.append({"budget": budget, "steps": len(steps), "chunk_tokens": budget - 32,
                      "step_us_mean": sum(us) / len(us), "step_us_max": max(us),
                      "prompt_prefill_ms": sum(us) / 1e3,
@@ -530,6 +605,54 @@ def run_sweep(args):
                      "step_roofline_frac_mean": sum(fr) / len(fr)})
         del ws, steps, outs, wsp
         torch.cuda.empty_cache()
+    grid = []
+    base_bytes = None
+    for chunk in free_ride_grid:
+        sc = workloads.free_ride(chunk, seed)
+        ws = workloads.WorkloadState(sc, device=dev)
+        inp = ws.step(0)
+        call = _fused_call(ws, inp, stream)
+        for _ in range(3):
+            flush.fill_(1)
+            call()
+        us = _time_calls(call, flush, stream, free_ride_steps)
+        m = inp["meta"]
+        c, roof = _roofline_entry(m, sc.shape, sum(us) / len(us), peaks)
+        if chunk == 0:
+            base_bytes = c["bytes"]
+        grid.append({"chunk": chunk, "step_us": sum(us) / len(us), "step_us_min": min(us),
+                     "step_roofline_frac": roof["frac"]})
+        del ws, inp, call
+        torch.cuda.empty_cache()
+    base = grid[0]["step_us"]
+    free = max(g["chunk"] for g in grid if g["step_us"] <= 1.05 * base)
+    # attention form of the estimate: C chunk tokens at offset P cost
+    # 4*D*Hq*(P*C + C*(C+1)/2) FLOPs; set that equal to the decodes' HBM time
+    # times the bf16 peak and solve for C
+    sh = workloads.LLAMA3_8B
+    per_pair = 4 * sh.head_dim * sh.num_q_heads
+    flops_budget = base_bytes / (peaks["hbm_gbs"] * 1e9) * peaks["bf16_tflops"] * 1e12
+    P = 3840
+    est = -P + math.sqrt(P * P + 2 * flops_budget / per_pair)
+    return {"budgets": rows,
+            "free_ride": {"decodes": 32, "chunk_offset": P, "decodes_alone_us": base,
+                          "measured_free_tokens": free, "criterion": "step within 5 % of the "
+                          "decodes-alone step", "formula_free_tokens": est,
+                          "formula": "C with 4*D*Hq*(P*C + C^2/2) / bf16 peak = decode bytes / "
+                                     "HBM peak", "grid": grid}}
+
+
+def run_sweep(args):
+    """The sweep alone, as its own JSON line."""
+    from chunked_prefill_paged_cpa_gb300 import ops
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    ops.load()
+    peaks, peak_src = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sw = measure_sweep(dev, flush, stream, peaks, args.seed)
     line = {"metric": "budget sweep: per-step us and total prompt prefill time", "unit": "us",
             "higher_is_better": False, "n_gpus": 1, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "budget_sweep", "prompt": 8192, "decodes": 32,
@@ -537,7 +660,7 @@ def run_sweep(args):
                        "page_size": 16, "seed": args.seed,
                        "l2": "flushed before every timed step",
                        "peaks": f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"},
-            "sweep": rows}
+            "sweep": sw}
     print(json.dumps(line), flush=True)
 
 
@@ -554,6 +677,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="budget sweep of an 8192-token prompt beside 32 decodes (one JSON line)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time only the headline workload (no per-workload table, no sweep)")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

@@ -139,19 +139,17 @@ extern "C" int cpa_kv_append(const void *k, const void *v, const int64_t *slot_m
 
 namespace cpa {
 
-// The step's new rows for a fused append (nullptr k: no append in this call).
-struct NewRows {
-  const void *k = nullptr, *v = nullptr;
-  const int64_t *slots = nullptr;
-};
-
 // Attention over the packed batch; with `nr.k` set the append of the step's
 // new rows is part of the call (fused into the attention kernels where they
 // take the shape, else one append launch ahead of them on the same stream).
-static int attention(const void *q, const void *k_cache, const void *v_cache,
-                     const int32_t *block_table, const int32_t *query_start_loc,
-                     const int32_t *seq_lens, int32_t num_seqs, float scale, void *out,
-                     void *stream, const cpa_desc *desc, const NewRows &nr) {
+// With clear_bytes > 0 the first clear_bytes of the workspace are zeroed on
+// the stream once every argument has passed its checks, just before the
+// first launch (a call that is rejected or has nothing to do leaves the
+// workspace untouched).
+int attention(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *query_start_loc,
+              const int32_t *seq_lens, int32_t num_seqs, float scale, void *out,
+              void *stream, const cpa_desc *desc, const NewRows &nr, size_t clear_bytes) {
   int rc = check_shape(desc);
   if (rc != CPA_OK) return rc;
   if (num_seqs < 0) return CPA_ERR_ARG;
@@ -207,6 +205,10 @@ static int attention(const void *q, const void *k_cache, const void *v_cache,
     if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
   }
   const bool launch_chunks = tc_chunks && !all_decode;
+  if (clear_bytes > 0) {
+    if (clear_bytes > desc->workspace_bytes) return CPA_ERR_WORKSPACE;
+    if (cudaMemsetAsync(desc->workspace, 0, clear_bytes, st) != cudaSuccess) return CPA_ERR_CUDA;
+  }
   if (nr.k) {
     if (w.fast_decode && (all_decode || tc_chunks)) {
       // fused: the chunk and decode kernels read the step's own rows from
@@ -278,7 +280,7 @@ extern "C" int cpa_attention_forward(const void *q, const void *k_cache, const v
                                      int32_t num_seqs, float scale, void *out, void *stream,
                                      const cpa_desc *desc) {
   return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs, scale,
-                   out, stream, desc, NewRows{});
+                   out, stream, desc, NewRows{}, 0);
 }
 
 extern "C" int cpa_append_attention_forward(const void *q, const void *k, const void *v,
@@ -299,7 +301,7 @@ extern "C" int cpa_append_attention_forward(const void *q, const void *k, const 
   nr.v = v;
   nr.slots = slot_mapping;
   return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs, scale,
-                   out, stream, desc, nr);
+                   out, stream, desc, nr, 0);
 }
 
 extern "C" int cpa_read_device_status(const cpa_desc *desc, void *stream, int32_t *status_out) {

@@ -76,6 +76,20 @@ struct AttnParams {
   float2 *part_ml;
 };
 
+// The step's new rows for a fused append (nullptr k: no append in this call).
+struct NewRows {
+  const void *k = nullptr, *v = nullptr;
+  const int64_t *slots = nullptr;
+};
+
+// The attention call behind every entry point (cpa_api.cu): validates the
+// arguments, optionally zeroes the first clear_bytes of the workspace on the
+// stream once they pass, then launches.
+int attention(const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_table, const int32_t *query_start_loc,
+              const int32_t *seq_lens, int32_t num_seqs, float scale, void *out,
+              void *stream, const cpa_desc *desc, const NewRows &nr, size_t clear_bytes);
+
 cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
                              void *k_cache, void *v_cache, int64_t num_tokens,
                              int Hkv, int D, int page_size, int64_t num_pages,

@@ -12,10 +12,13 @@
 // The array below lives in the device memory of every GPU that loads the
 // library, for as long as the process runs.  Host code must not hand the
 // array's name to a kernel: on the host that name is only a stand-in, not a
-// device address.  The real address is looked up once per device with
-// cudaGetSymbolAddress and cached.
-#include <mutex>
-
+// device address.  The real address is looked up with cudaGetSymbolAddress
+// on every call, for the device and context current at that moment: a cached
+// address would go stale when the module is loaded again (after
+// cudaDeviceReset, or in another context on the same device).  The lookup is
+// host-side and allocates nothing; only the first one in a context may have to
+// load the module, which is why the first call belongs before any stream
+// capture.
 #include "cpa_internal.cuh"
 
 namespace cpa {
@@ -23,31 +26,22 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CPA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up on the
-// first call made on that device).  Returns nullptr on failure.
-void *scratch_for_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-      cudaGetLastError();  // clear the (non-sticky) error so a later call can retry
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = ptr;
+// Device address of the scratch array in the current context, or nullptr.
+void *scratch_for_current_context() {
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+    cudaGetLastError();  // clear the (non-sticky) error so a later call can retry
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  return ptr;
 }
 
 }  // namespace
 }  // namespace cpa
 
 using namespace cpa;
+
+extern "C" size_t cpa_noalloc_scratch_bytes(void) { return CPA_NOALLOC_SCRATCH_BYTES; }
 
 extern "C" int cpa_attention_forward_noalloc(const void *q, const void *k_cache,
                                              const void *v_cache, const int32_t *block_table,
@@ -62,21 +56,34 @@ extern "C" int cpa_attention_forward_noalloc(const void *q, const void *k_cache,
   d.workspace_bytes = 0;
   const size_t need = cpa_workspace_bytes(&d, num_seqs);
   if (need == 0) {
-    // invalid description: let the regular entry point report the exact error
-    return cpa_attention_forward(q, k_cache, v_cache, block_table, query_start_loc,
-                                 seq_lens, num_seqs, scale, out, stream, &d);
+    // invalid description: the regular checks report the exact error
+    return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs,
+                     scale, out, stream, &d, NewRows{}, 0);
   }
   if (need > (size_t)CPA_NOALLOC_SCRATCH_BYTES) return CPA_ERR_WORKSPACE;
-  void *scratch = scratch_for_current_device();
+  void *scratch = scratch_for_current_context();
   if (!scratch) return CPA_ERR_CUDA;
-  // The merge counters and the status word must start at zero; a previous
-  // call on this device left the array as it finished (or was aborted), so
-  // clear them on the caller's stream before the launch.
-  const WorkspaceLayout w = workspace_layout(d, num_seqs);
-  if (cudaMemsetAsync(scratch, 0, w.part_o, (cudaStream_t)stream) != cudaSuccess)
-    return CPA_ERR_CUDA;
   d.workspace = scratch;
   d.workspace_bytes = CPA_NOALLOC_SCRATCH_BYTES;
-  return cpa_attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
-                               num_seqs, scale, out, stream, &d);
+  // The status word and the merge counters must start at zero; an earlier
+  // call left the array as it finished (or gave up).  They are cleared on the
+  // caller's stream only once the call has passed every check, right before
+  // its first launch.
+  const WorkspaceLayout w = workspace_layout(d, num_seqs);
+  return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs,
+                   scale, out, stream, &d, NewRows{}, w.part_o);
+}
+
+extern "C" int cpa_noalloc_read_device_status(void *stream, int32_t *status_out) {
+  if (!status_out) return CPA_ERR_ARG;
+  void *scratch = scratch_for_current_context();
+  if (!scratch) return CPA_ERR_CUDA;
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CPA_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, sizeof word, s) != cudaSuccess) return CPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CPA_ERR_CUDA;
+  *status_out = word ? CPA_ERR_DEVICE : CPA_OK;
+  return CPA_OK;
 }

@@ -79,6 +79,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.cpa_attention_forward_noalloc.restype = ctypes.c_int
         lib.cpa_read_device_status.argtypes = [D, P, ctypes.POINTER(I32)]
         lib.cpa_read_device_status.restype = ctypes.c_int
+        lib.cpa_noalloc_scratch_bytes.argtypes = []
+        lib.cpa_noalloc_scratch_bytes.restype = Z
+        lib.cpa_noalloc_read_device_status.argtypes = [P, ctypes.POINTER(I32)]
+        lib.cpa_noalloc_read_device_status.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -126,7 +130,20 @@ def cpa_attention_forward_noalloc(q, k_cache, v_cache, block_table, query_start_
                                                     ctypes.byref(desc)))
 
 
-CPA_NOALLOC_SCRATCH_BYTES = 16 << 20
+def cpa_noalloc_scratch_bytes() -> int:
+    """Size of the no-alloc entry point's built-in scratch array, as the
+    library was compiled."""
+    return int(load().cpa_noalloc_scratch_bytes())
+
+
+def cpa_noalloc_read_device_status(stream) -> int:
+    """Read and clear the status word of the no-alloc scratch array (waits
+    for ``stream``); CPA_OK or CPA_ERR_DEVICE."""
+    st = ctypes.c_int32(0)
+    rc = load().cpa_noalloc_read_device_status(stream, ctypes.byref(st))
+    if rc != CPA_OK:
+        raise CpaError(rc, "cpa_noalloc_read_device_status")
+    return int(st.value)
 
 
 def cpa_read_device_status(desc: CpaDesc, stream) -> int:

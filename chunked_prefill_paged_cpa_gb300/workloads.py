@@ -132,6 +132,18 @@ def budget_sweep(budget: int, seed: int = 0, prompt: int = 8192, decodes: int = 
                 budget, steps, seed, {"budget": budget, "prompt": prompt, "decodes": decodes})
 
 
+def free_ride(chunk: int, seed: int = 0) -> Scenario:
+    """The default step's 32 decodes (contexts ~U[512, 4096]) beside a chunk of
+    ``chunk`` tokens of the 8192-token prompt at offset 3840 (``chunk`` = 0:
+    the decodes alone).  A grid over ``chunk`` finds how many prompt tokens
+    ride along with the decode pass before the step gets slower ("Chunked
+    Prefill" (deepconcepts.dev), "Why a chunk can be nearly free")."""
+    L = synth.uniform_lengths(32, 512, 4096, seed * 1000 + 1)
+    waiting = [Request("P", 8192, 3840)] if chunk > 0 else []
+    return _run(f"free_ride_{chunk}", LLAMA3_8B, _decoders(L), waiting, 32 + chunk, 1, seed,
+                {"budget": 32 + chunk, "prompt": 8192, "offset": 3840, "chunk": chunk})
+
+
 NAMES = ["tiny", "page1_default", "large_budget", "long_context", "decode_only"]
 
 

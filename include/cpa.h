@@ -148,6 +148,10 @@ int cpa_append_attention_forward(const void *q, const void *k, const void *v,
  * loads the library, held until the process exits. */
 #define CPA_NOALLOC_SCRATCH_BYTES (16u << 20)
 
+/* CPA_NOALLOC_SCRATCH_BYTES as the library was built with it (for bindings
+ * that cannot read the macro). */
+size_t cpa_noalloc_scratch_bytes(void);
+
 /* Attention forward for callers that may not allocate device memory.  The
  * pages have no counterpart to this call: it is a library convenience.
  * Callers in this position include plugins inside a host runtime that owns
@@ -162,22 +166,32 @@ int cpa_append_attention_forward(const void *q, const void *k, const void *v,
  *  - Limit: the workspace this step would need, cpa_workspace_bytes(desc,
  *    num_seqs), must not exceed CPA_NOALLOC_SCRATCH_BYTES; larger steps are
  *    rejected with CPA_ERR_WORKSPACE before anything is launched.
- *  - Set-up: the first call on each device (with that device current) looks
- *    up the array's device address with cudaGetSymbolAddress and caches it;
- *    make that first call before any stream capture.  CPA_ERR_CUDA if the
- *    lookup fails.
+ *  - Set-up: every call looks up the array's device address in the current
+ *    context with cudaGetSymbolAddress (host-side; nothing is allocated).
+ *    The first call in a context may load the library's device code, so make
+ *    it before any stream capture.  CPA_ERR_CUDA if the lookup fails.
  *  - Sharing: every call on a device uses the same array, which keeps what the
- *    last call left in it.  Each call clears the merge counters and the
- *    status word on `stream` before its launch.  Calls whose work overlaps on
- *    the GPU (different streams, or different host threads) race on the
- *    array: serialise them.
- *  - The device status word of these calls is internal; use
- *    cpa_attention_forward with a workspace to read it. */
+ *    last call left in it.  Once a call has passed its argument checks it
+ *    clears the array's status word and merge counters on `stream`, right
+ *    before its first launch; a rejected or empty call touches nothing.
+ *    Calls whose work overlaps on the GPU (different streams, or different
+ *    host threads) race on the array: serialise them.
+ *  - Errors: those of cpa_attention_forward; out-of-range indices met by the
+ *    kernels are reported by cpa_noalloc_read_device_status. */
 int cpa_attention_forward_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                   const int32_t *block_table,
                                   const int32_t *query_start_loc, const int32_t *seq_lens,
                                   int32_t num_seqs, float scale, void *out, void *stream,
                                   const cpa_desc *desc);
+
+/* Synchronously read (and clear) the device status word of the no-alloc
+ * scratch array on the current device: CPA_OK, or CPA_ERR_DEVICE if the last
+ * cpa_attention_forward_noalloc call on this device met an out-of-range page
+ * index or gave up a bounded wait (its output is then incomplete).  Waits for
+ * `stream`; allocates nothing.  Test/debug helper, not meant for the hot
+ * path.  Returns CPA_ERR_ARG for a null status_out, CPA_ERR_CUDA if a CUDA
+ * call fails. */
+int cpa_noalloc_read_device_status(void *stream, int32_t *status_out);
 
 /* Synchronously read (and clear) the device status word held in the
  * workspace: CPA_OK, or CPA_ERR_DEVICE if a kernel since the last read met an

@@ -37,6 +37,20 @@ class OracleCache:
         return slots
 
 
+def oracle_append(st, meta=None):
+    """Append a ``make_step`` problem's new rows to its oracle cache through
+    the oracle's own slots (``oracle.slot_mapping`` on the block table),
+    checking on the way that the package's slot_mapping is the same bit for
+    bit.  Returns the oracle's slots."""
+    m = st["meta"] if meta is None else meta
+    slots = oracle.slot_mapping(m.block_table, m.query_start_loc, m.seq_lens,
+                                st["oracle_cache"].page_size)
+    assert torch.equal(slots, m.slot_mapping.cpu()), "package slots differ from the oracle's"
+    oracle.kv_append(st["oracle_cache"].k, st["oracle_cache"].v, st["k_new"], st["v_new"],
+                     slots)
+    return slots
+
+
 def oracle_state_for(ws):
     """Oracle cache holding each sequence's prefix as ``ws`` (a
     WorkloadState) has it before its first step."""

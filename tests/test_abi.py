@@ -119,3 +119,29 @@ def test_empty_step_is_a_no_op(lib):
     P = ctypes.c_void_p(4096)
     assert ops.cpa_kv_append(P, P, P, P, P, d, None) == ops.CPA_OK
     assert ops.cpa_attention_forward(P, P, P, P, P, P, 0, 0.1, P, None, d) == ops.CPA_OK
+
+
+def test_noalloc_scratch_size_is_exported(lib):
+    """The binding reads the no-alloc scratch size from the library; it must
+    be the header's value."""
+    text = open(os.path.join(ROOT, "include", "cpa.h")).read()
+    m = re.search(r"#define CPA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m, "CPA_NOALLOC_SCRATCH_BYTES not found in cpa.h"
+    assert ops.cpa_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
+def test_noalloc_rejects_bad_arguments_before_touching_the_device(lib):
+    P = ctypes.c_void_p(4096)
+    d = _desc()
+    f = ops.cpa_attention_forward_noalloc
+    assert f(P, P, P, P, P, P, -1, 0.1, P, None, d) == ops.CPA_ERR_ARG
+    assert f(P, P, P, P, P, P, 2, 0.1, P, None, _desc(head_dim=96)) == ops.CPA_ERR_UNSUPPORTED
+    assert f(P, P, P, P, P, P, 2, 0.1, P, None, _desc(max_pages_per_seq=0)) == ops.CPA_ERR_ARG
+    # far beyond the built-in scratch
+    assert f(P, P, P, P, P, P, 4096, 0.1, P, None,
+             _desc(num_tokens=4096, max_pages_per_seq=4096)) == ops.CPA_ERR_WORKSPACE
+    assert load_status_null(lib) == ops.CPA_ERR_ARG
+
+
+def load_status_null(lib):
+    return lib.cpa_noalloc_read_device_status(None, None)

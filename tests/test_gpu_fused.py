@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from chunked_prefill_paged_cpa_gb300 import ops, workloads
-from support import make_step
+from support import oracle_append, make_step
 from test_gpu_parity import assert_close, bits, check_full_config, gpu_step
 
 pytestmark = pytest.mark.gpu
@@ -75,7 +75,7 @@ def test_fused_call_equals_separate_calls_and_oracle(cuda_device, case):
     assert torch.equal(bits(out2), bits(out1)), "output"
     # and against the oracle: its own append, then the definition
     m, oc = st["meta"], st["oracle_cache"]
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     assert torch.equal(bits(kc2.cpu()), bits(oc.k)) and torch.equal(bits(vc2.cpu()), bits(oc.v))
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)

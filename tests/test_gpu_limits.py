@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from chunked_prefill_paged_cpa_gb300 import ops
-from support import make_step
+from support import oracle_append, make_step
 from test_gpu_parity import assert_close, bits, gpu_step
 
 pytestmark = pytest.mark.gpu
@@ -39,7 +39,7 @@ def test_largest_decode_batch_separate_and_fused(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(bits(kc2), bits(kc1)) and torch.equal(bits(vc2), bits(vc1))
     assert torch.equal(bits(out2), bits(out1))
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     assert torch.equal(bits(kc1.cpu()), bits(oc.k))
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)

@@ -12,7 +12,7 @@ import torch
 import oracle
 from chunked_prefill_paged_cpa_gb300 import ops, workloads
 from chunked_prefill_paged_cpa_gb300.batch import pages_for
-from support import make_step, oracle_state_for, to_np64
+from support import oracle_append, make_step, oracle_state_for, to_np64
 
 pytestmark = pytest.mark.gpu
 
@@ -163,7 +163,7 @@ def test_large_logit_jumps_rescale_and_redo(cuda_device):
            "v": st["v_new"].to(dev)}
     scale = 1 / math.sqrt(D)
     out, _ = gpu_step(k_cache, v_cache, inp, scale, Hq)
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)
     # the planted keys dominate: the output is close to the mean of their V rows
@@ -187,7 +187,7 @@ def test_every_chunk_kernel_shape(cuda_device, D, G):
            "v": st["v_new"].to(dev)}
     scale = 1 / math.sqrt(D)
     out, wsp = gpu_step(k_cache, v_cache, inp, scale, Hq)
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     assert torch.equal(bits(k_cache.cpu()), bits(oc.k))
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)
@@ -224,7 +224,7 @@ def test_decode_batches(cuda_device, case):
            "v": st["v_new"].to(dev)}
     scale = 1 / math.sqrt(D)
     out, wsp = gpu_step(k_cache, v_cache, inp, scale, Hq)
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)
     assert_close(out.cpu(), want, f"decode case {case}")
@@ -259,7 +259,7 @@ def test_multiple_chunks_per_step(cuda_device, case):
            "v": st["v_new"].to(dev)}
     scale = 1 / math.sqrt(128)
     out, wsp = gpu_step(k_cache, v_cache, inp, scale, 32)
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], m.slot_mapping)
+    oracle_append(st)
     want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
                             m.seq_lens, scale)
     assert_close(out.cpu(), want, f"multi-chunk case {case}")
@@ -274,8 +274,7 @@ def test_ones_values_give_ones_and_onehot_values_give_probabilities(cuda_device)
     q_lens, seq_lens, Hq, Hkv, D = [1, 20, 1], [1500, 60, 64], 8, 2, 64
     st = make_step(q_lens, seq_lens, Hq, Hkv, D, torch.bfloat16, seed=7)
     m, oc = st["meta"], st["oracle_cache"]
-    slots = m.slot_mapping
-    oracle.kv_append(oc.k, oc.v, st["k_new"], st["v_new"], slots)
+    oracle_append(st)
     ones = torch.ones_like(oc.v).to(dev)
     k_cache = oc.k.to(dev)
     wsp = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs)
@@ -328,12 +327,13 @@ def test_out_of_range_page_sets_status_without_fault(cuda_device):
     assert ops.device_status(k_cache, 4, bt.shape[1], wsp) == ops.CPA_ERR_DEVICE
 
 
-# ---- full-size workloads: sampled rows, per-sequence oracle ----------------
+# ---- full-size workloads: every row, per-sequence oracle -------------------
 
-def oracle_rows_for_seq(ws, rid, seq_len, q_len, rows):
+def oracle_rows_for_seq(ws, rid, seq_len, q_len, rows=None):
     """fp64 oracle output of rows ``rows`` (indices within the sequence's
-    q_len new tokens) computed from the generator's per-position tensors in a
-    fresh identity-paged host cache built by the oracle itself."""
+    q_len new tokens; all of them when None) computed from the generator's
+    per-position tensors in a fresh identity-paged host cache built by the
+    oracle itself (its own slots, its own append)."""
     sh = ws.sc.shape
     n = pages_for(seq_len, sh.page_size)
     kc = torch.full((n, sh.num_kv_heads, sh.page_size, sh.head_dim), float("nan"),
@@ -350,7 +350,31 @@ def oracle_rows_for_seq(ws, rid, seq_len, q_len, rows):
     return oracle.attention(q, kc, vc, bt, qsl, sl, sh.scale, rows=rows)
 
 
-def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24, fused=False):
+def oracle_step(ws, inp):
+    """fp64 oracle output of every query row of one step, [T, Hq, D]."""
+    m = inp["meta"]
+    sh = ws.sc.shape
+    qsl = m.query_start_loc.cpu().tolist()
+    want = np.empty((m.num_tokens, sh.num_q_heads, sh.head_dim), dtype=np.float64)
+    for i, s in enumerate(inp["plan"].seqs):
+        want[qsl[i]:qsl[i + 1]] = oracle_rows_for_seq(ws, s.rid, s.seq_len, s.q_len)
+    return want
+
+
+def check_step_against_oracle(name, ws, inp, out):
+    """Every row and head of a step's GPU output against the oracle: each
+    sequence on its own (max-abs and mean-abs), then the whole step."""
+    want = oracle_step(ws, inp)
+    got = out.float().cpu().numpy()
+    qsl = inp["meta"].query_start_loc.cpu().tolist()
+    for i, s in enumerate(inp["plan"].seqs):
+        assert_close(got[qsl[i]:qsl[i + 1]], want[qsl[i]:qsl[i + 1]],
+                     f"{name} seq {s.rid} ({s.kind}, q_len {s.q_len}, ctx {s.seq_len})")
+    assert_close(got, want, name)
+    return want
+
+
+def check_full_config(name, cuda_device, fused=False):
     sc = workloads.scenario(name)
     ws = workloads.WorkloadState(sc, device=cuda_device)
     inp = ws.step(0)
@@ -362,8 +386,10 @@ def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24, fu
                                            ws.k_cache, ws.v_cache, m.block_table,
                                            m.query_start_loc, m.seq_lens, sc.shape.scale, wsp)
     else:
-        out, _ = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, sc.shape.num_q_heads)
+        out, wsp = gpu_step(ws.k_cache, ws.v_cache, inp, sc.shape.scale, sc.shape.num_q_heads)
     torch.cuda.synchronize()
+    assert ops.device_status(ws.k_cache, sc.shape.num_q_heads, m.block_table.shape[1],
+                             wsp) == 0
     # paging bit-exact: the package's slots equal the oracle's, and the cache
     # holds the new rows at exactly those slots
     mc = m.to("cpu")
@@ -380,31 +406,115 @@ def check_full_config(name, cuda_device, n_decode_samples=6, n_chunk_rows=24, fu
     unused = (~used).nonzero().flatten().to(cuda_device)
     if unused.numel():
         assert torch.isnan(ws.k_cache[unused].float()).all()
-    # sampled rows against the oracle
-    g = torch.Generator().manual_seed(11)
-    qsl = mc.query_start_loc.tolist()
-    seqs = inp["plan"].seqs
-    dec = [i for i, s in enumerate(seqs) if s.kind == "decode"]
-    pick = [dec[int(j)] for j in torch.randperm(len(dec), generator=g)[:n_decode_samples]]
-    pre = [i for i, s in enumerate(seqs) if s.kind == "prefill"]
-    got_all, want_all = [], []
-    for i in pick + pre:
-        s = seqs[i]
-        if s.q_len == 1:
-            rows = [0]
-        else:
-            rows = sorted(set([0, 1, s.q_len - 1] +
-                              torch.randint(0, s.q_len, (n_chunk_rows,), generator=g).tolist()))
-        want = oracle_rows_for_seq(ws, s.rid, s.seq_len, s.q_len, rows)
-        got = out[[qsl[i] + r for r in rows]].float().cpu().numpy()
-        assert_close(got, want, f"{name} seq {s.rid}")
-        got_all.append(got)
-        want_all.append(want)
-    assert_close(np.concatenate([g_.ravel() for g_ in got_all]),
-                 np.concatenate([w.ravel() for w in want_all]), name)
+    # every row of every sequence against the oracle
+    check_step_against_oracle(name, ws, inp, out)
 
 
 @pytest.mark.parametrize("name", ["page1_default", "large_budget", "long_context",
-                                  "decode_only"])
+                                  "decode_only", "oneshot_8192"])
 def test_full_size_config(name, cuda_device):
     check_full_config(name, cuda_device)
+
+
+def test_chunked_prefill_equals_oneshot_at_full_size(cuda_device):
+    """The 8192-token prompt of the large-budget configuration prefilled as
+    four 2048-token chunks beside 4 decodes (four fused steps, each chunk
+    attending to the earlier chunks through the paged cache) equals the
+    one-shot 8192-token prefill of the same prompt: on the GPU, both within
+    tolerance of each other, and each, every row and head, within tolerance of
+    the fp64 oracle ("vllm-learning-book 05. Chunked Prefill", section 3;
+    "Chunked Prefill 技术深度解析", section 7.2).  The decodes of every step
+    are checked against the oracle too."""
+    from chunked_prefill_paged_cpa_gb300.batch import build_metadata
+    sc = workloads.scenario("large_budget_chunked")
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    sh = sc.shape
+    chunk_rows = []
+    for k in range(len(sc.plans)):
+        inp = ws.step(k)
+        m = inp["meta"]
+        assert sorted(m.q_lens) == [1, 1, 1, 1, 2048]
+        wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1],
+                                m.num_seqs)
+        out = ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping,
+                                           ws.k_cache, ws.v_cache, m.block_table,
+                                           m.query_start_loc, m.seq_lens, sh.scale, wsp)
+        torch.cuda.synchronize()
+        qsl = m.query_start_loc.cpu().tolist()
+        for i, s in enumerate(inp["plan"].seqs):
+            if s.kind == "decode":
+                want = oracle_rows_for_seq(ws, s.rid, s.seq_len, 1)
+                assert_close(out[qsl[i]:qsl[i + 1]].float().cpu(), want,
+                             f"step {k + 1} decode {s.rid}")
+            else:
+                assert s.rid == "P" and s.seq_len == 2048 * (k + 1)
+                chunk_rows.append(out[qsl[i]:qsl[i + 1]].clone())
+    chunked = torch.cat(chunk_rows)                       # prompt positions 0..8191
+    # the same prompt in one shot: its rows are already in the cache (the
+    # append writes the same bytes again), one 8192-token prefill entry
+    pos = torch.arange(8192)
+    meta = build_metadata([8192], [8192], [ws.paged.pages["P"]], 16,
+                          ws.num_pages).to(cuda_device)
+    kk, vv = ws.kv_rows("P", pos)
+    q = ws.q_rows("P", pos).to(cuda_device).contiguous()
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1)
+    one = ops.append_attention_forward(q, kk.to(cuda_device).contiguous(),
+                                       vv.to(cuda_device).contiguous(), meta.slot_mapping,
+                                       ws.k_cache, ws.v_cache, meta.block_table,
+                                       meta.query_start_loc, meta.seq_lens, sh.scale, wsp)
+    torch.cuda.synchronize()
+    assert_close(chunked.float().cpu(), one.float().cpu().double(),
+                 "chunked vs one-shot (GPU both)")
+    want = oracle_rows_for_seq(ws, "P", 8192, 8192)
+    assert_close(chunked.float().cpu(), want, "chunked prefill vs oracle")
+    assert_close(one.float().cpu(), want, "one-shot prefill vs oracle")
+
+
+def test_tiny_alternative_reading_sequence_twice_in_one_step(cuda_device):
+    """The tiny configuration's other reading: in step 3, A appears twice --
+    its last 32-token chunk (seq_len 96) and, in the same step, the decode of
+    its first generated token (position 96, seq_len 97), over the same block
+    table ("vllm-learning-book 05. Chunked Prefill", section 2: the first
+    output token is produced in the pass that finishes the prompt).  Run
+    through the separate calls, which allow a sequence more than once (the
+    fused call does not: its header requires each sequence at most once).
+    Checked against the oracle on every row, and A's decode against the last
+    row of a one-shot 97-token prefill."""
+    from chunked_prefill_paged_cpa_gb300.batch import build_metadata
+    sc = workloads.scenario("tiny")
+    ws = workloads.WorkloadState(sc, device=cuda_device)
+    oc = oracle_state_for(ws)
+    sh = sc.shape
+    for k in range(2):                                    # steps 1 and 2 as planned
+        inp = ws.step(k)
+        m = inp["meta"]
+        gpu_step(ws.k_cache, ws.v_cache, inp, sh.scale, sh.num_q_heads)
+        oc.append(m.block_table.cpu(), m.q_lens, m.seq_lens_list, inp["k"].cpu(),
+                  inp["v"].cpu())
+    # step 3, alternative reading: B decodes position 42; A's chunk 64..95 and
+    # A's decode at 96
+    pa = ws.paged.ensure("A", 97)
+    pb = ws.paged.ensure("B", 43)
+    q_lens, seq_lens = [1, 32, 1], [43, 96, 97]
+    meta = build_metadata(q_lens, seq_lens, [pb, pa, pa], 16, ws.num_pages)
+    qb = ws.q_rows("B", torch.tensor([42]))
+    qa = ws.q_rows("A", torch.arange(64, 97))
+    kb, vb = ws.kv_rows("B", torch.tensor([42]))
+    ka, va = ws.kv_rows("A", torch.arange(64, 97))
+    q = torch.cat([qb, qa]).to(cuda_device).contiguous()
+    k_new = torch.cat([kb, ka]).to(cuda_device).contiguous()
+    v_new = torch.cat([vb, va]).to(cuda_device).contiguous()
+    inp = {"meta": meta.to(cuda_device), "q": q, "k": k_new, "v": v_new}
+    out, wsp = gpu_step(ws.k_cache, ws.v_cache, inp, sh.scale, sh.num_q_heads)
+    torch.cuda.synchronize()
+    slots = oc.append(meta.block_table, q_lens, seq_lens, k_new.cpu(), v_new.cpu())
+    assert torch.equal(slots, meta.slot_mapping)
+    assert torch.equal(bits(ws.k_cache.cpu()), bits(oc.k))
+    assert torch.equal(bits(ws.v_cache.cpu()), bits(oc.v))
+    want = oracle.attention(q.cpu(), oc.k, oc.v, meta.block_table, meta.query_start_loc,
+                            meta.seq_lens, sh.scale)
+    assert_close(out.cpu(), want, "tiny step 3, A twice")
+    assert ops.device_status(ws.k_cache, sh.num_q_heads, meta.block_table.shape[1], wsp) == 0
+    # A's decode equals the last row of A's one-shot 97-token prefill
+    one = oracle_rows_for_seq(ws, "A", 97, 97, rows=[96])
+    assert_close(out[33:34].cpu(), one, "A's decode vs one-shot last row")
