@@ -269,7 +269,7 @@ def run_gpu(args, world, rank, local):
     eb = torch.empty((), dtype=sh.dtype).element_size()
     counts = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads,
                          sh.head_dim, eb)
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     out = torch.empty_like(inp["q"])
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -502,7 +502,7 @@ def _fused_call(ws, inp, stream):
     from chunked_prefill_paged_cpa_gb300 import ops
     sh = ws.sc.shape
     m = inp["meta"]
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     out = torch.empty_like(inp["q"])
 
     def call():
@@ -582,7 +582,8 @@ def measure_sweep(dev, flush, stream, peaks, seed, budgets=(256, 512, 2048, 1638
         steps = [ws.step(k) for k in range(len(sc.plans))]
         max_pages = max(x["meta"].block_table.shape[1] for x in steps)
         max_seqs = max(x["meta"].num_seqs for x in steps)
-        wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, max_pages, max_seqs)
+        wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, max_pages, max_seqs,
+                                 max(x["meta"].num_tokens for x in steps))
         outs = [torch.empty_like(x["q"]) for x in steps]
 
         def one(k):

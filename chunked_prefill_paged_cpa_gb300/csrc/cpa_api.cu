@@ -1,6 +1,6 @@
 // C ABI of libcpa: argument validation, workspace layout and launches.
 // Declared and documented in include/cpa.h.
-#include <mutex>
+#include <algorithm>
 
 #include "cpa_internal.cuh"
 
@@ -8,31 +8,7 @@ namespace cpa {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
-  WorkspaceLayout w{};
-  const int G = d.num_q_heads / d.num_kv_heads;
-  w.fast_decode = decode_fast_path(d.dtype, d.head_dim, G);
-  const int64_t max_keys = (int64_t)d.max_pages_per_seq * d.page_size;
-  w.max_splits = (int)((max_keys + kSplitKeys - 1) / kSplitKeys);
-  if (w.max_splits < 1) w.max_splits = 1;
-  size_t off = 256;  // header
-  w.counters = off;
-  off = align_up(off + sizeof(uint32_t) * (size_t)num_seqs * d.num_kv_heads, 256);
-  w.part_o = off;
-  size_t rows;  // partial rows of head_dim floats
-  if (w.fast_decode) {
-    rows = ((size_t)num_seqs * d.num_kv_heads + kDecodeMaxWorkers) * G;
-  } else {
-    rows = (size_t)num_seqs * d.num_q_heads * w.max_splits;
-  }
-  off = align_up(off + sizeof(float) * rows * d.head_dim, 256);
-  w.part_ml = off;
-  off = align_up(off + sizeof(float2) * rows, 256);
-  w.total = off;
-  return w;
-}
-
-int decode_grid(int device) {
+int sm_count(int device) {
   static int sms[64] = {};
   if (device < 0 || device >= 64) return 0;
   if (!sms[device]) {
@@ -46,34 +22,50 @@ int decode_grid(int device) {
   return sms[device];
 }
 
-// Per-device side stream and fork/join events used to run the chunk tiles
-// (tensor-bound) beside the decode stream (HBM-bound).  Created on first use;
-// they are CUDA objects, not device memory.  A mutex keeps the record/wait
-// sequence of concurrent host threads from interleaving.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-static SideStream g_side[64];
-static std::mutex g_side_mutex;
-
-static SideStream *side_stream(int device) {
-  if (device < 0 || device >= 64) return nullptr;
-  SideStream &ss = g_side[device];
-  if (!ss.stream) {
-    // highest priority: the chunk kernel's CTAs are dispatched ahead of the
-    // decode CTAs queued behind the SMs the decode kernel starts on
-    int lo = 0, hi = 0;
-    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
-    if (cudaStreamCreateWithPriority(&ss.stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
-      cudaGetLastError();
-      ss.stream = nullptr;
-      return nullptr;
-    }
+WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
+  WorkspaceLayout w{};
+  const int G = d.num_q_heads / d.num_kv_heads;
+  const int Hkv = d.num_kv_heads, D = d.head_dim;
+  w.step = step_path(d.dtype, D, G);
+  size_t off = 256;  // header
+  if (!w.step) {
+    const int64_t max_keys = (int64_t)d.max_pages_per_seq * d.page_size;
+    w.max_splits = (int)((max_keys + kSplitKeys - 1) / kSplitKeys);
+    if (w.max_splits < 1) w.max_splits = 1;
+    w.counters = off;
+    off = align_up(off + sizeof(uint32_t) * (size_t)num_seqs * Hkv, 256);
+    w.part_o = off;
+    const size_t rows = (size_t)num_seqs * d.num_q_heads * w.max_splits;
+    off = align_up(off + sizeof(float) * rows * D, 256);
+    w.part_ml = off;
+    off = align_up(off + sizeof(float2) * rows, 256);
+    w.total = off;
+    w.clear = w.part_o;  // header and counters
+    return w;
   }
-  return &ss;
+  // capacities for a persistent grid of up to kMaxStepGrid CTAs (one per SM)
+  const int64_t tok = d.num_tokens > 0 ? d.num_tokens : 0;
+  w.cap_dec = Hkv * num_seqs + 32 * kMaxStepGrid;
+  w.cap_chunk = (int)std::max<int64_t>(kMaxStepGrid,
+                                       (int64_t)Hkv * ((tok * G + 255) / 256 + num_seqs));
+  w.cap_split = kMaxStepGrid;
+  w.list = off;
+  off = align_up(off + (size_t)32 * (w.cap_dec + w.cap_chunk), 256);
+  w.dec_ctr = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)num_seqs * Hkv, 256);
+  w.chunk_ctr = off;
+  off = align_up(off + sizeof(uint32_t) * 2 * (size_t)w.cap_chunk, 256);
+  w.dec_o = off;
+  off = align_up(off + sizeof(float) * (size_t)w.cap_dec * G * D, 256);
+  w.dec_ml = off;
+  off = align_up(off + sizeof(float2) * (size_t)w.cap_dec * G, 256);
+  w.chunk_o = off;
+  off = align_up(off + sizeof(float) * (size_t)w.cap_split * 2 * 128 * D, 256);
+  w.chunk_ml = off;
+  off = align_up(off + sizeof(float2) * (size_t)w.cap_split * 2 * 128, 256);
+  w.total = off;
+  w.clear = 256;  // the status word; the plan kernel zeroes the rest it uses
+  return w;
 }
 
 // Shape checks shared by both calls.
@@ -186,90 +178,56 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
   p.scale_log2 = scale * 1.4426950408889634f;
   p.max_splits = w.max_splits;
   p.status = reinterpret_cast<uint32_t *>(ws);
-  p.counters = reinterpret_cast<uint32_t *>(ws + w.counters);
-  p.part_o = reinterpret_cast<float *>(ws + w.part_o);
-  p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
   cudaStream_t st = (cudaStream_t)stream;
-  const int G = p.Hq / p.Hkv;
-  const bool all_decode = (p.num_tokens == num_seqs);  // every q_len is 1
-  const bool tc_chunks = chunk_tc_path(desc->dtype, p.D, G);
-  if (tc_chunks && (int64_t)p.num_pages * p.Hkv * p.page_size >= INT32_MAX)
-    return CPA_ERR_UNSUPPORTED;  // tensor-map row coordinates are 32-bit
-  bool rows_for_decodes = true, rows_for_chunks = !all_decode;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
-  const int sms = decode_grid(dev);
-  if (sms <= 0) return CPA_ERR_CUDA;
-  if (w.fast_decode) {
+  int grid = 0;
+  if (w.step) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CPA_ERR_CUDA;
+    grid = std::min(sm_count(dev), kMaxStepGrid);
+    if (grid <= 0) return CPA_ERR_CUDA;
     if (num_seqs > kDecodeMaxSeqs) return CPA_ERR_UNSUPPORTED;
+    // tensor-map row coordinates and page-stream offsets are 32-bit
+    if ((int64_t)p.num_pages * p.Hkv * p.page_size >= INT32_MAX) return CPA_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * p.Hkv * p.max_pages > INT32_MAX) return CPA_ERR_UNSUPPORTED;
   }
-  const bool launch_chunks = tc_chunks && !all_decode;
   if (clear_bytes > 0) {
     if (clear_bytes > desc->workspace_bytes) return CPA_ERR_WORKSPACE;
     if (cudaMemsetAsync(desc->workspace, 0, clear_bytes, st) != cudaSuccess) return CPA_ERR_CUDA;
   }
-  if (nr.k) {
-    if (w.fast_decode && (all_decode || tc_chunks)) {
-      // fused: the chunk and decode kernels read the step's own rows from
-      // k/v; the decode kernel writes every new row into the cache
+  if (w.step) {
+    // One launch pair for the whole step: the plan (with the append when it
+    // is fused into the call), then the persistent step kernel.
+    StepWs sw{};
+    sw.hdr = reinterpret_cast<int *>(ws + 64);
+    sw.list = reinterpret_cast<int *>(ws + w.list);
+    sw.dec_ctr = reinterpret_cast<uint32_t *>(ws + w.dec_ctr);
+    sw.chunk_ctr = reinterpret_cast<uint32_t *>(ws + w.chunk_ctr);
+    sw.dec_o = reinterpret_cast<float *>(ws + w.dec_o);
+    sw.dec_ml = reinterpret_cast<float2 *>(ws + w.dec_ml);
+    sw.chunk_o = reinterpret_cast<float *>(ws + w.chunk_o);
+    sw.chunk_ml = reinterpret_cast<float2 *>(ws + w.chunk_ml);
+    sw.grid = grid;
+    if (nr.k) {
       p.fused = 1;
       p.k_new = nr.k;
       p.v_new = nr.v;
       p.slot_mapping = nr.slots;
-    } else {
-      const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
-      if (launch_kv_append(nr.k, nr.v, nr.slots, const_cast<void *>(k_cache),
-                           const_cast<void *>(v_cache), desc->num_tokens, p.Hkv, p.D,
-                           p.page_size, p.num_pages, eb, p.status, st) != cudaSuccess)
-        return CPA_ERR_CUDA;
     }
+    return launch_attention_step(p, sw, st) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
   }
-  if (launch_chunks && w.fast_decode) {
-    // Both kernels hold one CTA per SM.  The chunk tiles run on the side
-    // stream (highest priority, so their CTAs are placed first) and the
-    // decode kernel on the caller's stream takes every SM: dg CTAs start
-    // beside the chunk tiles, the rest as the chunk kernel's CTAs finish
-    // (with dg = 0 all of them, the page stream split evenly).  When the chunk
-    // items outnumber the SMs, the CTAs left with one item finish a wave
-    // early and the decodes run there.
-    const int cg = chunk_grid_estimate(p, sms);
-    int dg = sms - cg;
-    if (dg > kDecodeMaxWorkers / 8) dg = kDecodeMaxWorkers / 8;
-    {
-      std::lock_guard<std::mutex> lock(g_side_mutex);
-      SideStream *ss = side_stream(dev);
-      if (!ss) return CPA_ERR_CUDA;
-      if (cudaEventRecord(ss->fork, st) != cudaSuccess ||
-          cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
-        return CPA_ERR_CUDA;
-      if (launch_attention_chunk(p, cg, ss->stream) != cudaSuccess) return CPA_ERR_CUDA;
-      AttnParams pd = p;
-      pd.decode_early = dg;
-      pd.chunk_grid = cg;
-      const int gd = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
-      if (launch_attention_decode(pd, gd, st) != cudaSuccess) return CPA_ERR_CUDA;
-      if (cudaEventRecord(ss->join, ss->stream) != cudaSuccess ||
-          cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess)
-        return CPA_ERR_CUDA;
-    }
-    rows_for_decodes = rows_for_chunks = false;
-  } else {
-    if (w.fast_decode) {
-      int g2 = sms > kDecodeMaxWorkers / 8 ? kDecodeMaxWorkers / 8 : sms;
-      if (launch_attention_decode(p, g2, st) != cudaSuccess) return CPA_ERR_CUDA;
-      rows_for_decodes = false;
-    }
-    if (launch_chunks) {
-      if (launch_attention_chunk(p, chunk_grid_estimate(p, sms), st) != cudaSuccess)
-        return CPA_ERR_CUDA;
-      rows_for_chunks = false;
-    }
+  // row kernel: the append (if any) first, on the same stream
+  if (nr.k) {
+    const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
+    if (launch_kv_append(nr.k, nr.v, nr.slots, const_cast<void *>(k_cache),
+                         const_cast<void *>(v_cache), desc->num_tokens, p.Hkv, p.D,
+                         p.page_size, p.num_pages, eb, p.status, st) != cudaSuccess)
+      return CPA_ERR_CUDA;
   }
-  if (!rows_for_decodes && !rows_for_chunks) return CPA_OK;
-  p.rows_mode = (rows_for_decodes && rows_for_chunks) ? 0 : (rows_for_chunks ? 1 : 2);
-  cudaError_t e = launch_attention_rows(p, desc->dtype, st);
-  return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+  p.counters = reinterpret_cast<uint32_t *>(ws + w.counters);
+  p.part_o = reinterpret_cast<float *>(ws + w.part_o);
+  p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
+  p.rows_mode = 0;
+  return launch_attention_rows(p, desc->dtype, st) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }
 
 }  // namespace cpa

@@ -17,27 +17,60 @@ enum : uint32_t {
   STATUS_TIMEOUT = 4u,    // a bounded wait gave up
 };
 
-// Workspace layout (byte offsets from desc->workspace, all 256-aligned):
-//   [0, 256)   header: uint32 status word
-//   counters   uint32 [num_seqs * Hkv]   split-merge arrival counts
-//   part_o     split partial outputs (float), part_ml their (max, sum) pairs.
-// With the streaming decode kernel (bf16 fast path) a partial slot holds the
-// G rows of one (sequence, kv head) contribution and there are
-// num_seqs * Hkv + kDecodeMaxWorkers slots; otherwise the row kernel keeps
-// one slot per (sequence, query head, split).
+// Workspace layout (byte offsets from desc->workspace, all 256-aligned).
+// Both layouts start with a 256-byte header whose first word is the device
+// status word.
+//  - Row kernel (fp32 and shapes the step kernel does not take):
+//      counters  uint32 [num_seqs * Hkv]      split-merge arrival counts
+//      part_o / part_ml  one partial (o, (max, sum)) per (sequence, query
+//                        head, split of kSplitKeys keys)
+//  - Step kernel (bf16, head_dim 64/128, GQA group 1/2/4/8):
+//      header    status word; queue sizes, decode slice pages, ticket
+//      list      the step's work queue, one 32-byte entry per item
+//      dec_ctr   uint32 [num_seqs * Hkv]      decode segments' arrival counts
+//      chunk_ctr uint32 [2 * chunk units]     per (tile pair, tile) counts
+//      dec_o / dec_ml   one partial per decode slice: G rows x D, (max, sum)
+//      chunk_o / chunk_ml  one partial per split chunk unit: two 128-row tiles
+//    Capacities, for a grid of up to kMaxStepGrid CTAs: decode slices <=
+//    Hkv * num_seqs + 32 * kMaxStepGrid; chunk units <= max(kMaxStepGrid,
+//    Hkv * (ceil(num_tokens * G / 256) + num_seqs)); split chunk units <=
+//    kMaxStepGrid.  The plan kernel zeroes the counters and the ticket of
+//    every step, so nothing but the status word carries over between calls.
 struct WorkspaceLayout {
-  size_t counters, part_o, part_ml, total;
+  bool step;
+  size_t total;
+  size_t clear;  // bytes to zero before a call on a workspace in unknown state
+  // row kernel
+  size_t counters, part_o, part_ml;
   int max_splits;
-  bool fast_decode;
+  // step kernel
+  size_t list, dec_ctr, chunk_ctr, dec_o, dec_ml, chunk_o, chunk_ml;
+  int cap_dec, cap_chunk, cap_split;
 };
 
 // Keys handled by one split of a long decode in the row kernel.
 constexpr int kSplitKeys = 512;
-// Streaming decode kernel limits.
+// Sequences per step on the step kernel (its plan scans them in shared memory).
 constexpr int kDecodeMaxSeqs = 4096;
-constexpr int kDecodeMaxWorkers = 4096;  // CTAs x warps of its persistent grid
+// Largest persistent grid of the step kernel (one CTA per SM, capped here);
+// the workspace is sized for it, so its size is plain host arithmetic.
+constexpr int kMaxStepGrid = 256;
 
+// Layout for this description and at most num_seqs sequences.
 WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs);
+
+// Device pointers into the step kernel's workspace.
+struct StepWs {
+  int *hdr;            // [0] chunk units, [1] decode slices, [2] items, [3] pages per slice, [4] ticket
+  int *list;           // 8 ints per queue entry
+  uint32_t *dec_ctr;
+  uint32_t *chunk_ctr;
+  float *dec_o;
+  float2 *dec_ml;
+  float *chunk_o;
+  float2 *chunk_ml;
+  int grid;            // CTAs of the step kernel (one per SM)
+};
 
 struct AttnParams {
   const void *q;
@@ -55,17 +88,10 @@ struct AttnParams {
   float scale_log2;          // scale * log2(e): scores live in the log2 domain
   int max_splits;
   int rows_mode;              // row kernel: 0 all tokens, 1 only q_len > 1, 2 only q_len == 1
-  // Streaming decode kernel beside the chunk kernel: its first decode_early
-  // CTAs start at once, the rest as the chunk kernel's chunk_grid CTAs finish.
-  // The page stream is split between the two groups on the device so both end
-  // about together.  0 = every CTA starts at once (even split).
-  int decode_early;
-  int chunk_grid;
-  // Fused append (cpa_append_attention_forward): the step's new k/v rows
-  // [num_tokens][Hkv][D] and their cache slots.  The attention kernels take
-  // the step's own keys and values from k_new/v_new and the decode kernel also
-  // writes every new row into the cache.  fused = 0: the cache already holds
-  // them (cpa_kv_append ran first).
+  // Fused append (cpa_append_attention_forward, step kernel): the step's new
+  // k/v rows [num_tokens][Hkv][D] and their cache slots; the plan kernel
+  // copies them into the cache before the step kernel reads it.  fused = 0:
+  // the cache already holds them (cpa_kv_append ran first).
   int fused;
   const void *k_new;
   const void *v_new;
@@ -97,16 +123,12 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
 
 cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t stream);
 
-// Streaming split-KV decode kernel (bf16; head_dim 64/128; GQA group 2/4/8
-// with group * head_dim <= 512).
-bool decode_fast_path(int dtype, int D, int G);
-cudaError_t launch_attention_decode(const AttnParams &p, int grid, cudaStream_t stream);
-int decode_grid(int device);
+// Number of SMs of a device (cached); 0 if it cannot be queried.
+int sm_count(int device);
 
-// Prefill-chunk tiles on tcgen05 (bf16; head_dim 64/128; GQA group 1/2/4/8).
-bool chunk_tc_path(int dtype, int D, int G);
-cudaError_t launch_attention_chunk(const AttnParams &p, int grid, cudaStream_t stream);
-int chunk_grid_estimate(const AttnParams &p, int sms);
+// The step kernel (attn_step.cu): bf16, head_dim 64/128, GQA group 1/2/4/8.
+bool step_path(int dtype, int D, int G);
+cudaError_t launch_attention_step(const AttnParams &p, const StepWs &w, cudaStream_t stream);
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

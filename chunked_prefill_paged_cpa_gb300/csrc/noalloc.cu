@@ -71,7 +71,7 @@ extern "C" int cpa_attention_forward_noalloc(const void *q, const void *k_cache,
   // its first launch.
   const WorkspaceLayout w = workspace_layout(d, num_seqs);
   return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs,
-                   scale, out, stream, &d, NewRows{}, w.part_o);
+                   scale, out, stream, &d, NewRows{}, w.clear);
 }
 
 extern "C" int cpa_noalloc_read_device_status(void *stream, int32_t *status_out) {

@@ -184,9 +184,11 @@ def make_desc(k_cache: torch.Tensor, num_q_heads: int, num_tokens: int,
 
 
 def workspace_for(k_cache: torch.Tensor, num_q_heads: int, max_pages_per_seq: int,
-                  num_seqs: int) -> torch.Tensor:
-    """A zero-filled device workspace sized by cpa_workspace_bytes."""
-    desc = make_desc(k_cache, num_q_heads, 0, max_pages_per_seq)
+                  num_seqs: int, num_tokens: int) -> torch.Tensor:
+    """A zero-filled device workspace sized by cpa_workspace_bytes for steps of
+    at most ``num_seqs`` sequences and ``num_tokens`` packed tokens on the
+    current device."""
+    desc = make_desc(k_cache, num_q_heads, num_tokens, max_pages_per_seq)
     n = cpa_workspace_bytes(desc, num_seqs)
     if n == 0:
         raise CpaError(CPA_ERR_ARG, "cpa_workspace_bytes")

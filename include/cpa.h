@@ -77,11 +77,13 @@ typedef struct cpa_desc {
 /* Human-readable name of a cpa_status value (static string, never NULL). */
 const char *cpa_status_string(int status);
 
-/* Bytes of workspace cpa_attention_forward needs for at most `num_seqs`
- * sequences with this description.  Pure host arithmetic; returns 0 if the
- * description is invalid.  The workspace holds the split-KV partial results
- * (o, running max, running sum) of long decodes, the per-(sequence, kv head)
- * arrival counters of the in-launch merge, and a device status word. */
+/* Bytes of workspace cpa_attention_forward needs for steps of at most
+ * `num_seqs` sequences and desc->num_tokens packed tokens.  Pure host
+ * arithmetic; returns 0 if the description is invalid.  The workspace holds
+ * the step's work queue, the split-KV partial results (o, running max, running
+ * sum) of decode segments and of chunk tiles split over several CTAs, their
+ * arrival counters (zeroed by every call before use), and a device status
+ * word.  It is sized for a GPU of up to 256 SMs. */
 size_t cpa_workspace_bytes(const cpa_desc *desc, int32_t num_seqs);
 
 /* KV append: for every packed token t with slot = slot_mapping[t] >= 0, copy
@@ -118,7 +120,7 @@ int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cach
 /* KV append and attention forward of one step in one call: the same results
  * as cpa_kv_append(k, v, slot_mapping, k_cache, v_cache, desc, stream)
  * followed by cpa_attention_forward(...) on the same stream -- the cache holds
- * the same bytes afterwards and out the same values -- without the separate
+ * the same bytes afterwards and out the same values -- without a separate
  * append launch ("Chunked Prefill on an M5 Max", section "Wiring it into the
  * loop": appending is part of each chunk's fixed cost).
  *  - Arguments: those of the two calls; k, v [num_tokens][Hkv][D] in the
@@ -127,13 +129,12 @@ int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cach
  *    position in its sequence (block_table[s][pos / 16] * 16 + pos % 16);
  *    tokens with a negative slot are not written, and no query may attend to
  *    them.
- *  - Where the bf16 attention kernels take the shape (head_dim 64 or 128,
- *    GQA group 2, 4 or 8 with group * head_dim <= 512), the append is fused
- *    into them: the step's own keys and values are read from k/v, not from the
- *    cache, and the decode kernel writes every new row into its slot.  In
- *    that case each sequence may appear only once in the batch, and the cache
- *    rows this call writes are complete only when the call's work on `stream`
- *    has finished.  Otherwise the call launches the append and then the
+ *  - Where the step kernel takes the shape (bf16, head_dim 64 or 128, GQA
+ *    group 1, 2, 4 or 8), the step's planning kernel copies the new rows into
+ *    the cache while the attention kernel sets up, and the attention reads
+ *    them from the cache once that copy is complete: a sequence may appear
+ *    more than once in the batch (a chunk and a decode of the same sequence
+ *    in one step).  Otherwise the call launches the append and then the
  *    attention on `stream`.
  *  - Errors: those of the two calls; slots >= num_pages * page_size raise the
  *    device status word and are not written. */
@@ -144,9 +145,9 @@ int cpa_append_attention_forward(const void *q, const void *k, const void *v,
                                  void *out, void *stream, const cpa_desc *desc);
 
 /* Size of the scratch array built into the library for
- * cpa_attention_forward_noalloc: 16 MiB of device memory on every GPU that
+ * cpa_attention_forward_noalloc: 64 MiB of device memory on every GPU that
  * loads the library, held until the process exits. */
-#define CPA_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define CPA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* CPA_NOALLOC_SCRATCH_BYTES as the library was built with it (for bindings
  * that cannot read the macro). */
@@ -172,8 +173,9 @@ size_t cpa_noalloc_scratch_bytes(void);
  *    it before any stream capture.  CPA_ERR_CUDA if the lookup fails.
  *  - Sharing: every call on a device uses the same array, which keeps what the
  *    last call left in it.  Once a call has passed its argument checks it
- *    clears the array's status word and merge counters on `stream`, right
- *    before its first launch; a rejected or empty call touches nothing.
+ *    clears the array's status word (and the merge counters the call uses) on
+ *    `stream`, right before its first launch; a rejected or empty call
+ *    touches nothing.
  *    Calls whose work overlaps on the GPU (different streams, or different
  *    host threads) race on the array: serialise them.
  *  - Errors: those of cpa_attention_forward; out-of-range indices met by the

@@ -56,7 +56,7 @@ def _run_both(st, Hq, D, dev):
     kc1, vc1 = oc.k.to(dev), oc.v.to(dev)
     kc2, vc2 = kc1.clone(), vc1.clone()
     out1, _ = gpu_step(kc1, vc1, {"meta": md, "q": q, "k": k, "v": v}, scale, Hq)
-    wsp = ops.workspace_for(kc2, Hq, md.block_table.shape[1], md.num_seqs)
+    wsp = ops.workspace_for(kc2, Hq, md.block_table.shape[1], md.num_seqs, md.num_tokens)
     out2 = ops.append_attention_forward(q, k, v, md.slot_mapping, kc2, vc2, md.block_table,
                                         md.query_start_loc, md.seq_lens, scale, wsp)
     torch.cuda.synchronize()
@@ -100,7 +100,7 @@ def test_fused_out_of_range_slot_sets_status_without_fault(cuda_device):
     kc, vc = oc.k.to(dev), oc.v.to(dev)
     slots = m.slot_mapping.clone()
     slots[0] = kc.shape[0] * 16 + 5            # the first decode's token: out of range
-    wsp = ops.workspace_for(kc, 32, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(kc, 32, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     ops.append_attention_forward(st["q"].to(dev), st["k_new"].to(dev), st["v_new"].to(dev),
                                  slots, kc, vc, m.block_table, m.query_start_loc, m.seq_lens,
                                  1 / math.sqrt(128), wsp)

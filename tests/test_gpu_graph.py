@@ -35,7 +35,7 @@ def test_captured_step_replays_bit_for_bit(cuda_device):
 
     # eager reference
     kc, vc = k0.clone(), v0.clone()
-    ws_e = ops.workspace_for(kc, Hq, max_pages, m.num_seqs)
+    ws_e = ops.workspace_for(kc, Hq, max_pages, m.num_seqs, m.num_tokens)
     ops.kv_append(k, v, m.slot_mapping, kc, vc)
     out_e = ops.attention_forward(q, kc, vc, m.block_table, m.query_start_loc, m.seq_lens,
                                   scale, ws_e)
@@ -43,7 +43,7 @@ def test_captured_step_replays_bit_for_bit(cuda_device):
 
     # capture on static buffers (warm-up first, as graph capture requires)
     kg, vg = k0.clone(), v0.clone()
-    ws_g = ops.workspace_for(kg, Hq, max_pages, m.num_seqs)
+    ws_g = ops.workspace_for(kg, Hq, max_pages, m.num_seqs, m.num_tokens)
     out_g = torch.empty_like(out_e)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -87,13 +87,13 @@ def test_captured_fused_call_replays_bit_for_bit(cuda_device):
     max_pages = m.block_table.shape[1]
 
     kc, vc = k0.clone(), v0.clone()
-    ws_e = ops.workspace_for(kc, Hq, max_pages, m.num_seqs)
+    ws_e = ops.workspace_for(kc, Hq, max_pages, m.num_seqs, m.num_tokens)
     out_e = ops.append_attention_forward(q, k, v, m.slot_mapping, kc, vc, m.block_table,
                                          m.query_start_loc, m.seq_lens, scale, ws_e)
     torch.cuda.synchronize()
 
     kg, vg = k0.clone(), v0.clone()
-    ws_g = ops.workspace_for(kg, Hq, max_pages, m.num_seqs)
+    ws_g = ops.workspace_for(kg, Hq, max_pages, m.num_seqs, m.num_tokens)
     out_g = torch.empty_like(out_e)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())

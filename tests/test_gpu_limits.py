@@ -33,7 +33,7 @@ def test_largest_decode_batch_separate_and_fused(cuda_device):
     kc1, vc1 = oc.k.to(dev), oc.v.to(dev)
     kc2, vc2 = kc1.clone(), vc1.clone()
     out1, wsp1 = gpu_step(kc1, vc1, {"meta": md, "q": q, "k": k, "v": v}, scale, 32)
-    wsp2 = ops.workspace_for(kc2, 32, md.block_table.shape[1], md.num_seqs)
+    wsp2 = ops.workspace_for(kc2, 32, md.block_table.shape[1], md.num_seqs, md.num_tokens)
     out2 = ops.append_attention_forward(q, k, v, md.slot_mapping, kc2, vc2, md.block_table,
                                         md.query_start_loc, md.seq_lens, scale, wsp2)
     torch.cuda.synchronize()
@@ -54,7 +54,7 @@ def test_one_more_sequence_than_supported_is_refused(cuda_device):
     dev = cuda_device
     m, oc = st["meta"].to(dev), st["oracle_cache"]
     kc, vc = oc.k.to(dev), oc.v.to(dev)
-    wsp = ops.workspace_for(kc, 32, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(kc, 32, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     q, k, v = st["q"].to(dev), st["k_new"].to(dev), st["v_new"].to(dev)
     before_k, before_v = kc.clone(), vc.clone()
     with pytest.raises(ops.CpaError) as e:

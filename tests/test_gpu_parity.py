@@ -40,7 +40,7 @@ def gpu_step(k_cache, v_cache, inp, scale, Hq, workspace=None):
     m = inp["meta"]
     ops.kv_append(inp["k"], inp["v"], m.slot_mapping, k_cache, v_cache)
     if workspace is None:
-        workspace = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs)
+        workspace = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     out = ops.attention_forward(inp["q"], k_cache, v_cache, m.block_table,
                                 m.query_start_loc, m.seq_lens, scale, workspace)
     return out, workspace
@@ -90,7 +90,7 @@ def test_tiny_chunked_equals_oneshot_on_gpu(cuda_device):
     kk, vv = ws2.kv_rows("A", pos)
     write_positions(ws2.k_cache, ws2.v_cache, pl, pos, kk, vv)
     meta = build_metadata([97], [97], [pl], 16, ws2.num_pages).to(cuda_device)
-    wsp = ops.workspace_for(ws2.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1)
+    wsp = ops.workspace_for(ws2.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1, meta.num_tokens)
     one = ops.attention_forward(ws2.q_rows("A", pos).to(cuda_device).contiguous(),
                                 ws2.k_cache, ws2.v_cache, meta.block_table,
                                 meta.query_start_loc, meta.seq_lens, sh.scale, wsp)
@@ -277,7 +277,7 @@ def test_ones_values_give_ones_and_onehot_values_give_probabilities(cuda_device)
     oracle_append(st)
     ones = torch.ones_like(oc.v).to(dev)
     k_cache = oc.k.to(dev)
-    wsp = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(k_cache, Hq, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     md = m.to(dev)
     out = ops.attention_forward(st["q"].to(dev), k_cache, ones, md.block_table,
                                 md.query_start_loc, md.seq_lens, 0.125, wsp)
@@ -316,7 +316,7 @@ def test_out_of_range_page_sets_status_without_fault(cuda_device):
     md = m.to(dev)
     bt = md.block_table.clone()
     bt[0, 1] = 10 ** 6                     # not a page of the pool
-    wsp = ops.workspace_for(k_cache, 4, bt.shape[1], 2)
+    wsp = ops.workspace_for(k_cache, 4, bt.shape[1], 2, md.num_tokens)
     ops.attention_forward(st["q"].to(dev), k_cache, v_cache, bt, md.query_start_loc,
                           md.seq_lens, 0.125, wsp)
     assert ops.device_status(k_cache, 4, bt.shape[1], wsp) == ops.CPA_ERR_DEVICE
@@ -381,7 +381,7 @@ def check_full_config(name, cuda_device, fused=False):
     m = inp["meta"]
     if fused:
         wsp = ops.workspace_for(ws.k_cache, sc.shape.num_q_heads, m.block_table.shape[1],
-                                m.num_seqs)
+                                m.num_seqs, m.num_tokens)
         out = ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping,
                                            ws.k_cache, ws.v_cache, m.block_table,
                                            m.query_start_loc, m.seq_lens, sc.shape.scale, wsp)
@@ -435,7 +435,7 @@ def test_chunked_prefill_equals_oneshot_at_full_size(cuda_device):
         m = inp["meta"]
         assert sorted(m.q_lens) == [1, 1, 1, 1, 2048]
         wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1],
-                                m.num_seqs)
+                                m.num_seqs, m.num_tokens)
         out = ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping,
                                            ws.k_cache, ws.v_cache, m.block_table,
                                            m.query_start_loc, m.seq_lens, sh.scale, wsp)
@@ -457,7 +457,7 @@ def test_chunked_prefill_equals_oneshot_at_full_size(cuda_device):
                           ws.num_pages).to(cuda_device)
     kk, vv = ws.kv_rows("P", pos)
     q = ws.q_rows("P", pos).to(cuda_device).contiguous()
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, meta.block_table.shape[1], 1, meta.num_tokens)
     one = ops.append_attention_forward(q, kk.to(cuda_device).contiguous(),
                                        vv.to(cuda_device).contiguous(), meta.slot_mapping,
                                        ws.k_cache, ws.v_cache, meta.block_table,

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _fused(ws, inp):
     sh = ws.sc.shape
     m = inp["meta"]
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     out = ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping,
                                        ws.k_cache, ws.v_cache, m.block_table,
                                        m.query_start_loc, m.seq_lens, sh.scale, wsp)

@@ -34,7 +34,7 @@ def _prepare(name, device):
     m = inp["meta"]
     sh = sc.shape
     ops.kv_append(inp["k"], inp["v"], m.slot_mapping, ws.k_cache, ws.v_cache)
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
     assert wsp.numel() <= ops.cpa_noalloc_scratch_bytes()
     ref = ops.attention_forward(inp["q"], ws.k_cache, ws.v_cache, m.block_table,
                                 m.query_start_loc, m.seq_lens, sh.scale, wsp)
