@@ -83,17 +83,21 @@ struct StepCfg {
   static constexpr int OFF_Q = 0;                // two query tiles
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * KV_BYTES;
-  // decode, inside the query-tile region: Q^T (16 rows) and each pipeline's
-  // P^T (16 rows x 128 keys), 1 KB aligned
-  static constexpr int OFF_QT = OFF_Q;
-  static constexpr int OFF_PT = OFF_Q + 4096;    // + 4096 * pipeline
+  // decode, inside the query-tile region (1 KB aligned): two Q^T buffers (16
+  // rows each, alternate items), each pipeline's P^T (16 rows x 128 keys),
+  // and a third V stage
+  static constexpr int QT_BYTES = PANELS * kDecN * 128;
+  static constexpr int OFF_QT = OFF_Q;           // + QT_BYTES * buffer
+  static constexpr int OFF_PT = OFF_Q + 2 * QT_BYTES;  // + 4096 * pipeline
+  static constexpr int OFF_VX = OFF_Q + 16384;
   // The decode PV uses M = 128 rows of V^T; at head_dim 64 its upper half reads
   // the next 2 KB (never used): keep that inside the allocation.
   static constexpr int PAD = D == 64 ? 2048 : 0;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES + PAD;
   static constexpr int BAR_BYTES = 2048;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // barriers and scratch, 1 KB alignment
-  static_assert(OFF_PT + 2 * 4096 <= OFF_K, "decode buffers overflow the query region");
+  static_assert(OFF_PT + 2 * 4096 <= OFF_VX && OFF_VX + KV_BYTES <= OFF_K,
+                "decode buffers overflow the query region");
   static_assert(SMEM <= 232448, "more shared memory than a CTA can have");
 };
 
@@ -109,11 +113,12 @@ struct WorkItem {
 };
 
 struct Bars {
-  uint64_t q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
-      o_final[2];
+  uint64_t q_full[2], q_empty[2], k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2],
+      p_full[2], o_final[2];
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   uint64_t wg_bar[2];            // softmax warpgroup syncs (128 arrivals)
   uint64_t hand_off, release;    // decode pipelines' merge (128 arrivals each)
+  uint64_t mma_done[2];          // each issuer's MMAs drained before TMEM is freed
   uint32_t tmem_base;
   uint32_t mma_lock;             // held by the issuer queueing a batch of MMAs
   int bcast[2];
@@ -443,6 +448,40 @@ __device__ __forceinline__ bool wg_sync(uint64_t *bar, uint32_t &phase) {
   return __all_sync(0xffffffffu, ok);
 }
 
+// The V stages in the order the item's tiles use them.  Chunk items cycle
+// through stages 0 and 1, decode items through 0, 1 and 2 (the third lives in
+// the query-tile region, which decode items do not fill).  Every role replays
+// the same sequence, item by item, so all agree on each tile's stage and on
+// how many times that stage was filled before.
+struct VRing {
+  int next = 0, v0 = 0, nst = 2;
+  uint32_t c0 = 0, c1 = 0, c2 = 0;  // fills of each stage before this item
+  __device__ __forceinline__ void begin(int kind) {
+    nst = kind == KIND_DECODE ? 3 : 2;
+    if (next >= nst) next = 0;
+    v0 = next;
+  }
+  // (constant divisors: 2 or 3)
+  __device__ __forceinline__ int mod(int x) const { return nst == 2 ? (x & 1) : x - 3 * (x / 3); }
+  __device__ __forceinline__ int div(int x) const { return nst == 2 ? (x >> 1) : x / 3; }
+  __device__ __forceinline__ int stage(int b) const { return mod(v0 + b); }
+  // 0-based fill index of tile b's stage
+  __device__ __forceinline__ uint32_t use(int b) const {
+    const int st = stage(b);
+    return (st == 0 ? c0 : (st == 1 ? c1 : c2)) + (uint32_t)div(b);
+  }
+  __device__ __forceinline__ void end(int n) {
+    auto add = [&](int st) -> uint32_t {
+      const int first = mod(st - v0 + nst);
+      return (st < nst && first < n) ? (uint32_t)(1 + div(n - 1 - first)) : 0u;
+    };
+    c0 += add(0);
+    c1 += add(1);
+    c2 += add(2);
+    next = mod(v0 + n);
+  }
+};
+
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUtensorMap tm_q,
@@ -458,17 +497,20 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
   unsigned char *sV = smem + C::OFF_V;
   Bars *bs = reinterpret_cast<Bars *>(smem + C::OFF_BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto v_stage = [&](int st) -> unsigned char * {
+    return st < 2 ? sV + st * C::KV_BYTES : smem + C::OFF_VX;
+  };
 
   if (tid == 0) {
-    ptx::mbar_init(&bs->q_full, 1);
-    ptx::mbar_init(&bs->q_empty, 2);
     for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&bs->k_full[i], 1);
       ptx::mbar_init(&bs->k_empty[i], 2);
-    }
-    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bs->v_full[i], 1);
       ptx::mbar_init(&bs->v_empty[i], 2);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&bs->q_full[i], 1);
+      ptx::mbar_init(&bs->q_empty[i], 2);
       ptx::mbar_init(&bs->s_full[i], 1);
       ptx::mbar_init(&bs->p_full[i], 128);
       ptx::mbar_init(&bs->o_final[i], 1);
@@ -480,6 +522,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     }
     ptx::mbar_init(&bs->hand_off, 128);
     ptx::mbar_init(&bs->release, 128);
+    ptx::mbar_init(&bs->mma_done[0], 1);
+    ptx::mbar_init(&bs->mma_done[1], 1);
     ptx::fence_mbar_init();
     bs->mma_lock = 0u;
   }
@@ -501,6 +545,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       ptx::prefetch_tmap(&tm_v);
     }
     const ItemDesc *list = reinterpret_cast<const ItemDesc *>(w.list);
+    // every lane polls; the warp moves on (or gives up) together
+    auto uwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity));
+    };
     auto claim = [&]() -> int {
       int t = 0;
       if (lane == 0) t = atomicAdd(w.hdr + 4, 1);
@@ -515,7 +563,11 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       return true;
     };
     uint32_t kvc = 0;  // K/V tiles loaded so far by this CTA
-    uint32_t issued_k = 0, issued_v = 0;
+    uint32_t issued_k = 0;
+    int64_t vlast0 = -1, vlast1 = -1, vlast2 = -1;  // last fill issued into each V stage
+    int qlast = -1;                                  // item of the last query load issued
+    VRing vr;
+    int prev_kind = KIND_DONE;
     bool ok = true;
     int n = 0;
     ItemDesc dsc;
@@ -532,7 +584,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         it.kind = KIND_DONE;
       }
       const int slot = n % kItemSlots;
-      if (n >= kItemSlots && !ptx::mbar_wait(&bs->item_empty[slot], ((n / kItemSlots) - 1) & 1)) {
+      if (n >= kItemSlots && !uwait(&bs->item_empty[slot], ((n / kItemSlots) - 1) & 1)) {
         ok = false;
         break;
       }
@@ -544,27 +596,38 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       if (it.kind == KIND_DONE) break;
       int tn = 0;
       if (lane == 0) tn = atomicAdd(w.hdr + 4, 1);  // the next ticket, in flight meanwhile
-      // the query buffers are free once every MMA of the previous item completed
-      if (n > 0 && !ptx::mbar_wait(&bs->q_empty, (n - 1) & 1)) { ok = false; break; }
+      // Query buffers: item n uses set n & 1.  A decode item's Q^T buffer is
+      // free once item n - 2's MMAs completed; a chunk's query tiles cover
+      // the whole region, so next to a chunk item n - 1's MMAs must be done too.
+      const int qb = n & 1;
+      if (n >= 2 && !uwait(&bs->q_empty[qb], ((n - 2) >> 1) & 1)) { ok = false; break; }
+      if (n >= 1 && (it.kind == KIND_CHUNK || prev_kind == KIND_CHUNK) &&
+          !uwait(&bs->q_empty[qb ^ 1], ((n - 1) >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      prev_kind = it.kind;
+      qlast = n;
+      vr.begin(it.kind);
       if (lane == 0) {
         if (it.kind == KIND_CHUNK) {
           const int nq = (it.n_mine[0] > 0) + (it.n_mine[1] > 0);
-          ptx::mbar_arrive_expect_tx(&bs->q_full, nq * C::Q_BYTES);
+          ptx::mbar_arrive_expect_tx(&bs->q_full[qb], nq * C::Q_BYTES);
           for (int i = 0; i < 2; ++i) {
             if (it.n_mine[i] == 0) continue;
 #pragma unroll
             for (int pl = 0; pl < C::PANELS; ++pl)
               ptx::tma_load_3d(sQ + i * C::Q_BYTES + pl * BM * 128, &tm_q, pl * 64, it.g * G,
-                               it.qs + (2 * it.mp + i) * TM, &bs->q_full);
+                               it.qs + (2 * it.mp + i) * TM, &bs->q_full[qb]);
           }
         } else {
           // Q^T: the G query rows of the token, [panel][16 rows][64] (rows
           // G..15 are never read back)
-          ptx::mbar_arrive_expect_tx(&bs->q_full, C::PANELS * G * 128);
+          ptx::mbar_arrive_expect_tx(&bs->q_full[qb], C::PANELS * G * 128);
 #pragma unroll
           for (int pl = 0; pl < C::PANELS; ++pl)
-            ptx::tma_load_3d(sQ + C::OFF_QT + pl * kDecN * 128, &tm_qd, pl * 64, it.g * G, it.qs,
-                             &bs->q_full);
+            ptx::tma_load_3d(sQ + C::OFF_QT + qb * C::QT_BYTES + pl * kDecN * 128, &tm_qd,
+                             pl * 64, it.g * G, it.qs, &bs->q_full[qb]);
         }
       }
       // page ids of the item, 32 at a time in this warp's registers (lane l
@@ -614,7 +677,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       for (int t = 0; t <= it.n_tiles; ++t) {
         if (t < it.n_tiles) {
           const uint32_t kc = kvc + t, st = kc % C::KST;
-          if (kc >= C::KST && !ptx::mbar_wait(&bs->k_empty[st], ((kc / C::KST) - 1) & 1)) {
+          if (kc >= C::KST && !uwait(&bs->k_empty[st], ((kc / C::KST) - 1) & 1)) {
             ok = false;
             break;
           }
@@ -622,16 +685,18 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           issued_k = kc + 1;
         }
         if (t >= 1) {
-          const uint32_t vc = kvc + t - 1, st = vc % C::VST;
-          if (vc >= C::VST && !ptx::mbar_wait(&bs->v_empty[st], ((vc / C::VST) - 1) & 1)) {
+          const int st = vr.stage(t - 1);
+          const uint32_t u = vr.use(t - 1);
+          if (u >= 1 && !uwait(&bs->v_empty[st], (u - 1) & 1)) {
             ok = false;
             break;
           }
-          load_tile(sV + st * C::KV_BYTES, true, &bs->v_full[st], t - 1);
-          issued_v = vc + 1;
+          load_tile(v_stage(st), true, &bs->v_full[st], t - 1);
+          if (st == 0) vlast0 = u; else if (st == 1) vlast1 = u; else vlast2 = u;
         }
       }
       if (!ok) break;
+      vr.end(it.n_tiles);
       kvc += it.n_tiles;
       ++n;
       tn = __shfl_sync(0xffffffffu, tn, 0);
@@ -643,8 +708,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         // let the copies still in flight land before the CTA leaves
         for (uint32_t c = issued_k > C::KST ? issued_k - C::KST : 0; c < issued_k; ++c)
           ptx::mbar_wait(&bs->k_full[c % C::KST], (c / C::KST) & 1, 1u << 16);
-        for (uint32_t c = issued_v > C::VST ? issued_v - C::VST : 0; c < issued_v; ++c)
-          ptx::mbar_wait(&bs->v_full[c % C::VST], (c / C::VST) & 1, 1u << 16);
+        if (vlast0 >= 0) ptx::mbar_wait(&bs->v_full[0], (uint32_t)vlast0 & 1, 1u << 16);
+        if (vlast1 >= 0) ptx::mbar_wait(&bs->v_full[1], (uint32_t)vlast1 & 1, 1u << 16);
+        if (vlast2 >= 0) ptx::mbar_wait(&bs->v_full[2], (uint32_t)vlast2 & 1, 1u << 16);
+        if (qlast >= 0) ptx::mbar_wait(&bs->q_full[qlast & 1], (qlast >> 1) & 1, 1u << 16);
       }
       __syncwarp();
     }
@@ -671,13 +738,15 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     constexpr uint32_t idesc_pv_d = ptx::idesc_bf16_f32(128, kDecN, true, false);
     const uint32_t tS = tmem + ti * 128, tO = tmem + 256 + ti * 128;
     constexpr int KS = D / 16, VS = BN / 16;
-    uint64_t qdesc[KS], kdesc[C::KST][KS], vdesc[C::VST][VS], qtdesc[KS], ptdesc[VS];
+    uint64_t qdesc[KS], kdesc[C::KST][KS], vdesc[3][VS], qtdesc[2][KS], ptdesc[VS];
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int o = (ks >> 2) * BM * 128 + (ks & 3) * 32;  // panel, 16-element step
       qdesc[ks] = ptx::smem_desc_sw128(sQ + ti * C::Q_BYTES + o, 16, 1024);
-      qtdesc[ks] = ptx::smem_desc_sw128(sQ + C::OFF_QT + (ks >> 2) * kDecN * 128 + (ks & 3) * 32, 16,
-                                        1024);
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        qtdesc[b][ks] = ptx::smem_desc_sw128(
+            sQ + C::OFF_QT + b * C::QT_BYTES + (ks >> 2) * kDecN * 128 + (ks & 3) * 32, 16, 1024);
 #pragma unroll
       for (int st = 0; st < C::KST; ++st)
         kdesc[st][ks] = ptx::smem_desc_sw128(sK + st * C::KV_BYTES + o, 16, 1024);
@@ -685,25 +754,54 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
 #pragma unroll
     for (int ks = 0; ks < VS; ++ks) {
 #pragma unroll
-      for (int st = 0; st < C::VST; ++st)
-        vdesc[st][ks] = ptx::smem_desc_sw128(sV + st * C::KV_BYTES + ks * C::PAGE_BYTES,
-                                             kPage * 128, 1024);
+      for (int st = 0; st < 3; ++st)
+        vdesc[st][ks] = ptx::smem_desc_sw128(v_stage(st) + ks * C::PAGE_BYTES, kPage * 128, 1024);
       ptdesc[ks] = ptx::smem_desc_sw128(
           sQ + C::OFF_PT + ti * 4096 + (ks >> 2) * kDecN * 128 + (ks & 3) * 32, 16, 1024);
     }
     uint32_t kvm = 0;   // K/V tiles loaded so far for this CTA (all roles agree)
     uint32_t pcnt = 0;  // P tiles of this slot consumed
+    VRing vr;
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n % kItemSlots;
-      if (!ptx::mbar_wait(&bs->item_full[slot], (n / kItemSlots) & 1)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->item_full[slot], (n / kItemSlots) & 1))) {
+        ok = false;
+        break;
+      }
       const WorkItem it = bs->items[slot];
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&bs->item_empty[slot]);
       if (it.kind == KIND_DONE) break;
       const int n_mine = (ti ? it.n_mine[1] : it.n_mine[0]), n_other = (ti ? it.n_mine[0] : it.n_mine[1]);
+      const int qb = n & 1;
+      const bool dec = it.kind == KIND_DECODE;
+      vr.begin(it.kind);
       if (lane == 0) {
-        if (it.kind == KIND_CHUNK) {
+        // Every K/V fill is observed by both issuers, in tile order: the one
+        // that reads it releases it with a commit after its MMAs; the other
+        // waits until it has landed and releases it with a plain arrival.
+        // So neither ever waits on a stage's barrier for a fill more than one
+        // ahead of the last it observed, where the parity could not tell the
+        // two apart (consecutive fills of a stage can belong to different
+        // issuers: decode blocks alternate between them, and a chunk's later
+        // tiles may be read by one query tile only).
+        auto ack_k1 = [&](int t) -> bool {  // observe K fill of tile t, release it
+          const uint32_t kc = kvm + t;
+          if (!ptx::mbar_wait(&bs->k_full[kc % C::KST], (kc / C::KST) & 1)) return false;
+          ptx::mbar_arrive(&bs->k_empty[kc % C::KST]);
+          return true;
+        };
+        auto ack_v1 = [&](int t) -> bool {  // observe V fill of tile t, release it
+          const int st = vr.stage(t);
+          if (!ptx::mbar_wait(&bs->v_full[st], vr.use(t) & 1)) return false;
+          ptx::mbar_arrive(&bs->v_empty[st]);
+          return true;
+        };
+        ok = ptx::mbar_wait(&bs->q_full[qb], (n >> 1) & 1);
+        if (!dec) {
+          // chunk: this tile reads K/V tiles 0 .. n_mine-1 (the later ones, if
+          // any, only the other tile reads)
           auto issue_qk = [&](uint32_t kvidx) {
             const uint32_t st = kvidx % C::KST;
 #pragma unroll
@@ -715,11 +813,6 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
               }
             }
           };
-          auto release_k = [&](uint32_t kvidx) {
-            ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
-            if ((int)(kvidx - kvm) >= n_other) ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
-          };
-          ok = ptx::mbar_wait(&bs->q_full, n & 1);
           if (ok && n_mine > 0) {
             ok = ptx::mbar_wait(&bs->k_full[kvm % C::KST], (kvm / C::KST) & 1) && lock();
             if (ok) {
@@ -727,15 +820,15 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
               issue_qk(kvm);
               unlock();
               ptx::mma_commit(&bs->s_full[ti]);
-              release_k(kvm);
+              ptx::mma_commit(&bs->k_empty[kvm % C::KST]);
             }
           }
           for (int j = 0; ok && j < n_mine; ++j) {
             const uint32_t kv = kvm + j;
-            const int vst = kv % C::VST;
+            const int vst = vr.stage(j);
             const bool more = j + 1 < n_mine;
             if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) ||
-                !ptx::mbar_wait(&bs->v_full[vst], (kv / C::VST) & 1) ||
+                !ptx::mbar_wait(&bs->v_full[vst], vr.use(j) & 1) ||
                 (more && !ptx::mbar_wait(&bs->k_full[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) ||
                 !lock()) {
               ok = false;
@@ -744,7 +837,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             ++pcnt;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int s2 = 0; s2 < C::VST; ++s2) {
+            for (int s2 = 0; s2 < 2; ++s2) {
               if (vst == s2) {
 #pragma unroll
                 for (int ks = 0; ks < VS; ++ks)
@@ -755,16 +848,23 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             unlock();
             if (more) {
               ptx::mma_commit(&bs->s_full[ti]);
-              release_k(kv + 1);
+              ptx::mma_commit(&bs->k_empty[(kv + 1) % C::KST]);
             } else {
               ptx::mma_commit(&bs->o_final[ti]);
             }
             ptx::mma_commit(&bs->v_empty[vst]);
-            if (j >= n_other) ptx::mma_commit(&bs->v_empty[vst]);
+          }
+          // The tiles only the other tile reads, observed and released in the
+          // order the producer issues them (K_t before V_{t-1}): it may need
+          // one of these releases before it can issue a fill waited on here.
+          for (int t = n_mine; ok && t <= it.n_tiles; ++t) {
+            if (t < it.n_tiles) ok = ack_k1(t);
+            if (ok && t > n_mine) ok = ack_v1(t - 1);
           }
         } else {
-          // decode: this pipeline takes blocks ti, ti + 2, ...; the other
-          // pipeline reads none of them, so every release counts twice
+          // decode: this pipeline reads blocks ti, ti + 2, ...; the other
+          // pipeline's blocks are observed and released in tile order as this
+          // one passes them
           auto issue_qk = [&](uint32_t kvidx) {
             const uint32_t st = kvidx % C::KST;
 #pragma unroll
@@ -772,33 +872,34 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
               if (st == (uint32_t)s3) {
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks)
-                  ptx::mma_bf16_ss(tS, kdesc[s3][ks], qtdesc[ks], idesc_qk_d, ks > 0 ? 1u : 0u);
+                  ptx::mma_bf16_ss(tS, kdesc[s3][ks], qb ? qtdesc[1][ks] : qtdesc[0][ks], idesc_qk_d,
+                                   ks > 0 ? 1u : 0u);
               }
             }
           };
-          auto release_k = [&](uint32_t kvidx) {
-            ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
-            ptx::mma_commit(&bs->k_empty[kvidx % C::KST]);
-          };
-          ok = ptx::mbar_wait(&bs->q_full, n & 1);
           if (ok && n_mine > 0) {
             const uint32_t kv0 = kvm + ti;
-            ok = ptx::mbar_wait(&bs->k_full[kv0 % C::KST], (kv0 / C::KST) & 1) && lock();
+            ok = (ti == 0 || ack_k1(0)) &&
+                 ptx::mbar_wait(&bs->k_full[kv0 % C::KST], (kv0 / C::KST) & 1) && lock();
             if (ok) {
               ptx::tc_fence_after();
               issue_qk(kv0);
               unlock();
               ptx::mma_commit(&bs->s_full[ti]);
-              release_k(kv0);
+              ptx::mma_commit(&bs->k_empty[kv0 % C::KST]);
             }
           }
           for (int j = 0; ok && j < n_mine; ++j) {
-            const uint32_t kv = kvm + ti + 2 * j;
-            const int vst = kv % C::VST;
+            const int t = ti + 2 * j;
+            const uint32_t kv = kvm + t;
+            const int vst = vr.stage(t);
             const bool more = j + 1 < n_mine;
-            if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) ||
-                !ptx::mbar_wait(&bs->v_full[vst], (kv / C::VST) & 1) ||
-                (more && !ptx::mbar_wait(&bs->k_full[(kv + 2) % C::KST], ((kv + 2) / C::KST) & 1)) ||
+            // the other pipeline's V of block t - 1 and K of block t + 1 come
+            // before this one's V of block t and K of block t + 2
+            if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) || (t > 0 && !ack_v1(t - 1)) ||
+                !ptx::mbar_wait(&bs->v_full[vst], vr.use(t) & 1) ||
+                (more && (!ack_k1(t + 1) ||
+                          !ptx::mbar_wait(&bs->k_full[(kv + 2) % C::KST], ((kv + 2) / C::KST) & 1))) ||
                 !lock()) {
               ok = false;
               break;
@@ -806,7 +907,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             ++pcnt;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int s2 = 0; s2 < C::VST; ++s2) {
+            for (int s2 = 0; s2 < 3; ++s2) {
               if (vst == s2) {
 #pragma unroll
                 for (int ks = 0; ks < VS; ++ks)
@@ -818,23 +919,40 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             unlock();
             if (more) {
               ptx::mma_commit(&bs->s_full[ti]);
-              release_k(kv + 2);
+              ptx::mma_commit(&bs->k_empty[(kv + 2) % C::KST]);
             } else {
               ptx::mma_commit(&bs->o_final[ti]);
             }
             ptx::mma_commit(&bs->v_empty[vst]);
-            ptx::mma_commit(&bs->v_empty[vst]);
+          }
+          // the other pipeline's blocks after this one's last (K_t before
+          // V_{t-1}, as the producer issues them)
+          const int done = n_mine > 0 ? ti + 2 * (n_mine - 1) + 1 : 0;  // tiles passed
+          for (int t = done; ok && t <= it.n_tiles; ++t) {
+            if (t < it.n_tiles && (t & 1) != ti) ok = ack_k1(t);
+            if (ok && t > done && ((t - 1) & 1) != ti) ok = ack_v1(t - 1);
           }
         }
-        if (ok && n_mine > 0) {
-          ptx::mma_commit(&bs->q_empty);
-          if (n_other == 0) ptx::mma_commit(&bs->q_empty);
+        if (ok) {
+          if (n_mine > 0) {
+            ptx::mma_commit(&bs->q_empty[qb]);
+          } else {
+            ptx::mbar_arrive(&bs->q_empty[qb]);
+          }
         }
+        (void)n_other;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      vr.end(it.n_tiles);
       kvm += it.n_tiles;
     }
-    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
+    if (lane == 0) {
+      if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
+      // every MMA this thread issued has completed before TMEM is freed
+      ptx::mma_commit(&bs->mma_done[ti]);
+      ptx::mbar_wait(&bs->mma_done[ti], 0, 1u << 20);
+    }
+    __syncwarp();
   } else {
     // ------------------------------- softmax ------------------------------------
     const int ti = warp >> 2;                 // query tile slot / decode pipeline
@@ -844,7 +962,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     const uint32_t tS = tmem + ti * 128 + lane_off;
     const uint32_t tO = tmem + 256 + ti * 128 + lane_off;
     const float sl2 = p.scale_log2;
-    uint32_t scnt = 0, ocnt = 0, kvb = 0, wgp = 0, nfin = 0;
+    uint32_t scnt = 0, ocnt = 0, wgp = 0, nfin = 0;
+    VRing vr;
     bool ok = true;
     for (int n = 0; ok; ++n) {
       const int slot = n % kItemSlots;
@@ -858,6 +977,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       if (it.kind == KIND_DONE) break;
       const int n_mine = (ti ? it.n_mine[1] : it.n_mine[0]);
       const int ctx = it.ctx;
+      vr.begin(it.kind);
       if (it.kind == KIND_CHUNK) {
         const int q_len = it.q_len;
         const int tok = (2 * it.mp + ti) * TM + r / G;  // index within the chunk
@@ -924,14 +1044,13 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           // Cache slots at or past ctx in the last page may hold anything (NaN
           // included) and 0 * NaN is NaN inside PV: zero those V rows first.
           if (key0 + BN > ctx) {
-            const uint32_t kv = kvb + j;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1))) {
+            const int vst = vr.stage(j);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[vst], vr.use(j) & 1))) {
               ok = false;
               break;
             }
             if (r >= ctx - key0 && r < it.n_pages * kPage - key0) {
-              unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + (r / kPage) * C::PAGE_BYTES +
-                                    (r % kPage) * 128;
+              unsigned char *vrow = v_stage(vst) + (r / kPage) * C::PAGE_BYTES + (r % kPage) * 128;
 #pragma unroll
               for (int pl = 0; pl < C::PANELS; ++pl)
 #pragma unroll
@@ -944,7 +1063,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           ptx::tc_fence_before();
           ptx::mbar_arrive(&bs->p_full[ti]);
         }
-        kvb += it.n_tiles;
+        vr.end(it.n_tiles);
         if (!ok || n_mine == 0) continue;
         // epilogue: O / l, or this unit's partial and, from the last unit of
         // the pair to finish, the merge of all of them
@@ -1060,7 +1179,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
 #pragma unroll
         for (int q = 0; q < G; ++q) { m_run[q] = -INFINITY; l_part[q] = 0.f; }
         const int key_lim = min(ctx, it.page_end * kPage);
-        unsigned char *pt = sQ + C::OFF_PT + ti * 4096;
+        unsigned char *pt = smem + C::OFF_PT + ti * 4096;
         for (int j = 0; j < n_mine; ++j, ++scnt) {
           const int blk = ti + 2 * j;
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->s_full[ti], scnt & 1))) { ok = false; break; }
@@ -1110,14 +1229,13 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           // cache slots past ctx in the sequence's last page: zero their V rows
           const int key0 = (it.page0 + 8 * blk) * kPage;
           if (key0 + BN > ctx && key0 < it.n_pages * kPage) {
-            const uint32_t kv = kvb + blk;
-            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[kv % C::VST], (kv / C::VST) & 1))) {
+            const int vst = vr.stage(blk);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[vst], vr.use(blk) & 1))) {
               ok = false;
               break;
             }
             if (key >= ctx && key < min(it.n_pages, it.page_end) * kPage) {
-              unsigned char *vrow = sV + (kv % C::VST) * C::KV_BYTES + (r / kPage) * C::PAGE_BYTES +
-                                    (r % kPage) * 128;
+              unsigned char *vrow = v_stage(vst) + (r / kPage) * C::PAGE_BYTES + (r % kPage) * 128;
 #pragma unroll
               for (int pl = 0; pl < C::PANELS; ++pl)
 #pragma unroll
@@ -1130,7 +1248,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           ptx::tc_fence_before();
           ptx::mbar_arrive(&bs->p_full[ti]);
         }
-        kvb += it.n_tiles;
+        vr.end(it.n_tiles);
         if (!ok) break;
         if (n_mine > 0) {
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->o_final[ti], ocnt & 1))) { ok = false; break; }
