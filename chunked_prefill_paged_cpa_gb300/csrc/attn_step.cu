@@ -23,13 +23,11 @@
 //                into several slices is merged the same way by its last slice.
 //
 // A small plan kernel runs first (programmatic dependent launch: the step
-// kernel's prologue overlaps it).  It enumerates the items, interleaves the
-// two kinds in one queue (chunk units spread over the front part of the
-// queue, so the long tensor-bound units start early while decode slices keep
-// HBM busy from the start), zeroes the queue ticket and every merge counter of
-// this step, and -- when the append is fused into the call -- copies the
-// step's new K/V rows into the cache, so the step kernel reads every key and
-// value from the cache.
+// kernel's prologue overlaps it).  It enumerates the items and queues them
+// longest first (chunk units, then decode slices by size), zeroes the queue
+// ticket and every merge counter of this step, and -- when the append is fused
+// into the call -- copies the step's new K/V rows into the cache, so the step
+// kernel reads every key and value from the cache.
 //
 // Step kernel, per CTA (352 threads, one CTA per SM):
 //   warp 8     producer: claims items from the queue, publishes them to the
@@ -67,9 +65,12 @@ constexpr int kItemSlots = 4;
 constexpr int kDecN = 16;        // N of the decode MMAs: the G query rows, padded
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPlanThreads = 1024;
-// Chunk units are spread over the first kFrontDen / kFrontNum of the decode
-// slices in the queue (a structural ordering choice: long items first).
-constexpr int kFrontNum = 3, kFrontDen = 2;
+// A tile pair's KV range is split over several units only into pieces of at
+// least this many KV tiles (8192 keys): each unit pays a query load, a
+// pipeline fill and a partial-result merge.
+constexpr int kUnitTiles = 64;
+// Decode slices are queued longest first, bucketed by their 8-page blocks.
+constexpr int kSizeBuckets = 1024;
 
 enum : int { KIND_CHUNK = 0, KIND_DECODE = 1, KIND_DONE = 2 };
 
@@ -234,15 +235,14 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     long long tp = 0, tt = 0, tq = 0;
     for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tt += s_red[i][1]; tq += s_red[i][2]; }
     const long long grid = w.grid;
-    // decode pages per slice: about four slices per CTA, at least 16 pages,
-    // at most 128 unless the slice capacity of the workspace needs more
+    // decode pages per slice: about two slices per CTA (every slice pays a
+    // pipeline fill and a finalisation; a segment cut into pieces also pays a
+    // merge), at least 16 pages
     auto c8 = [](long long x) { return (x + 7) / 8 * 8; };
-    long long P = c8((tp + 4 * grid - 1) / (4 * grid));
-    const long long hi = max(128ll, c8((tp + 32 * grid - 1) / (32 * grid)));
-    P = max(16ll, min(P, hi));
-    // chunk units per tile pair: enough to give every CTA one when the
-    // chunks have fewer tile pairs than CTAs
-    const long long nu = (tq == 0 || tq >= grid) ? 1 : max(1ll, grid / tq);
+    const long long P = max(16ll, c8((tp + 2 * grid - 1) / (2 * grid)));
+    // at most this many units per tile pair (only when the chunks have fewer
+    // tile pairs than CTAs; the split-unit partials hold kMaxStepGrid units)
+    const long long nu = (tq == 0 || tq >= grid) ? 1 : max(1ll, (long long)kMaxStepGrid / tq);
     s_par[0] = (int)P;
     s_par[1] = (int)nu;
     (void)tt;
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
       cd += Hkv * ceil_div(ceil_div(ctx, kPage), P);
     } else {
       const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-      const int nkv_max = max(tile_kv<G>(ctx, q_len, mt - 1), tile_kv<G>(ctx, q_len, 2 * (npair - 1)));
-      cc += Hkv * npair * min(nu, nkv_max);
+      const int nkv_max = tile_kv<G>(ctx, q_len, mt - 1);
+      cc += Hkv * npair * min(nu, ceil_div(nkv_max, kUnitTiles));
     }
   }
   int id = cd, ic = cc;
@@ -291,18 +291,18 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
         rd += Hkv * ceil_div(ceil_div(ctx, kPage), P);
       } else {
         const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-        const int nkv_max = max(tile_kv<G>(ctx, q_len, mt - 1), tile_kv<G>(ctx, q_len, 2 * (npair - 1)));
-        rc += Hkv * npair * min(nu, nkv_max);
+        const int nkv_max = tile_kv<G>(ctx, q_len, mt - 1);
+        rc += Hkv * npair * min(nu, ceil_div(nkv_max, kUnitTiles));
       }
     }
     if (tid == kPlanThreads - 1) { s_dec[S] = rd; s_chk[S] = rc; }
   }
   __syncthreads();
   const int Nd = s_dec[S], Nc = s_chk[S];
-  // The two lists interleaved: chunk unit k is preceded by a(k) decode slices
-  // and decode slice i by b(i) chunk units, with a non-decreasing, so the
-  // positions k + a(k) and i + b(i) are a permutation of the queue.
-  const long long an = (long long)Nd * kFrontDen, ad = (long long)kFrontNum * max(Nc, 1);
+  // Queue order, longest items first: the chunk units (tile pairs from the
+  // last, which see the most keys), then the decode slices by size.  The
+  // dynamic queue then fills the SMs the chunk units leave free with decode
+  // slices from the start, and ends on the shortest slices.
   auto search = [&](const int *base, int k) {  // last s with base[s] <= k
     int lo = 0, hi = S - 1;
     while (lo < hi) {
@@ -317,12 +317,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
     const int ctx = seq_ctx(p, s, q_len);
     const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-    const int nkv_max = max(tile_kv<G>(ctx, q_len, mt - 1), tile_kv<G>(ctx, q_len, 2 * (npair - 1)));
-    const int nus = min(nu, nkv_max);
+    const int nus = min(nu, ceil_div(tile_kv<G>(ctx, q_len, mt - 1), kUnitTiles));
     const int local = k - s_chk[s];
     const int pair = local / nus, u = local - pair * nus;
     const int mp = npair - 1 - pair / Hkv, g = pair % Hkv;  // later tiles (more keys) first
-    const long long a = Nd == 0 ? 0 : (long long)k * an / ad;
     ItemDesc d;
     d.s_kind = s;
     d.qs = qs;
@@ -332,27 +330,64 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     d.a = u | (nus << 16);
     d.b = k;
     d.c = k - u;
-    reinterpret_cast<ItemDesc *>(w.list)[k + a] = d;
+    reinterpret_cast<ItemDesc *>(w.list)[k] = d;
   }
-  for (int i = tid; i < Nd; i += kPlanThreads) {
-    const int s = search(s_dec, i);
-    const int qs = __ldg(p.query_start_loc + s);
-    const int ctx = seq_ctx(p, s, 1);
-    const int n = ceil_div(ctx, kPage), ks = ceil_div(n, P);
+  // decode slices, longest first: histogram of their 8-page blocks, bases
+  // in descending order, then each slice takes the next place of its bucket
+  __shared__ int s_hist[kSizeBuckets];
+  for (int b = tid; b < kSizeBuckets; b += kPlanThreads) s_hist[b] = 0;
+  __syncthreads();
+  auto slice_geom = [&](int i, int &s, int &g, int &piece, int &p0, int &p1, int &ks, int &ctx) {
+    s = search(s_dec, i);
+    ctx = seq_ctx(p, s, 1);
+    const int n = ceil_div(ctx, kPage);
+    ks = ceil_div(n, P);
     const int local = i - s_dec[s];
-    const int g = local / ks, piece = local - g * ks;
-    long long b = Nc;
-    if (Nc > 0 && Nd > 0) b = min((long long)Nc, ((long long)(i + 1) * ad + an - 1) / an);
+    g = local / ks;
+    piece = local - g * ks;
+    p0 = (int)((long long)piece * n / ks);
+    p1 = (int)((long long)(piece + 1) * n / ks);
+  };
+  auto bucket = [&](int p0, int p1) { return min(ceil_div(p1 - p0, 8), kSizeBuckets - 1); };
+  for (int i = tid; i < Nd; i += kPlanThreads) {
+    int s, g, piece, p0, p1, ks, ctx;
+    slice_geom(i, s, g, piece, p0, p1, ks, ctx);
+    atomicAdd(&s_hist[bucket(p0, p1)], 1);
+  }
+  __syncthreads();
+  {
+    // exclusive scan from the largest bucket down (one bucket per thread)
+    static_assert(kSizeBuckets == kPlanThreads, "one size bucket per plan thread");
+    const int b = kSizeBuckets - 1 - tid;  // thread 0 takes the largest bucket
+    const int c = s_hist[b];
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wd[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int i = 0; i < warp; ++i) base += s_wd[i];
+    __syncthreads();
+    s_hist[b] = base + incl - c;
+  }
+  __syncthreads();
+  for (int i = tid; i < Nd; i += kPlanThreads) {
+    int s, g, piece, p0, p1, ks, ctx;
+    slice_geom(i, s, g, piece, p0, p1, ks, ctx);
+    const int r = atomicAdd(&s_hist[bucket(p0, p1)], 1);  // place in the decode order
     ItemDesc d;
     d.s_kind = s | (KIND_DECODE << 30);
-    d.qs = qs;
+    d.qs = __ldg(p.query_start_loc + s);
     d.ctx = ctx;
     d.q_len = ks;
     d.g_x = g | (piece << 8);
-    d.a = (int)((long long)piece * n / ks);
-    d.b = (int)((long long)(piece + 1) * n / ks);
-    d.c = i;
-    reinterpret_cast<ItemDesc *>(w.list)[i + b] = d;
+    d.a = p0;
+    d.b = p1;
+    d.c = i;  // partial slot: the slice's own index, whatever its place
+    reinterpret_cast<ItemDesc *>(w.list)[Nc + r] = d;
   }
   // merge counters of this step start at zero; so does the queue ticket
   for (int x = tid; x < S * Hkv; x += kPlanThreads) w.dec_ctr[x] = 0u;
@@ -570,6 +605,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     int prev_kind = KIND_DONE;
     bool ok = true;
     int n = 0;
+    // The next item is claimed only once every copy of the current one has
+    // been issued: the CTA is then close to free (which keeps the queue's
+    // longest-first order dynamic), and the claim's latency hides behind the
+    // consumers' last queued tiles.
     ItemDesc dsc;
     bool have = fetch(claim(), dsc);
     for (;;) {
@@ -594,8 +633,6 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       }
       __syncwarp();
       if (it.kind == KIND_DONE) break;
-      int tn = 0;
-      if (lane == 0) tn = atomicAdd(w.hdr + 4, 1);  // the next ticket, in flight meanwhile
       // Query buffers: item n uses set n & 1.  A decode item's Q^T buffer is
       // free once item n - 2's MMAs completed; a chunk's query tiles cover
       // the whole region, so next to a chunk item n - 1's MMAs must be done too.
@@ -699,8 +736,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       vr.end(it.n_tiles);
       kvc += it.n_tiles;
       ++n;
-      tn = __shfl_sync(0xffffffffu, tn, 0);
-      have = fetch(tn, dsc);
+      have = fetch(claim(), dsc);
     }
     if (!ok) {
       if (lane == 0) {
