@@ -164,6 +164,10 @@ struct ItemDesc {
 // Plan kernel: block 0 builds the queue; blocks >= 1 append the step's new
 // K/V rows into the cache when the append is fused into the call.
 
+// dynamic shared memory of the plan: per sequence its first token, query
+// length, context, two exclusive bases and a queue place
+inline size_t plan_smem_bytes(int num_seqs) { return sizeof(int) * (6 * (size_t)num_seqs + 2); }
+
 template <int G>
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParams p,
                                                                   const StepWs w) {
@@ -198,73 +202,74 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     return;
   }
 
-  __shared__ int s_dec[kDecodeMaxSeqs + 1];   // exclusive bases of each sequence's slices
-  __shared__ int s_chk[kDecodeMaxSeqs + 1];   // ... and of its chunk units
-  __shared__ long long s_red[kPlanThreads / 32][3];
-  __shared__ int s_par[4];
+  // Block 0: the queue.  Every sequence's metadata is read once (coalesced)
+  // into shared memory; totals and per-sequence counts come from block scans;
+  // the decode slices are ordered longest first by a count per size bucket
+  // (one atomic per sequence); the entries are then written in parallel.
+  extern __shared__ int plan_smem[];
   const int S = p.num_seqs, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.Hkv;
+  int *sq_qs = plan_smem, *sq_len = sq_qs + S, *sq_ctx = sq_len + S;
+  int *s_dec = sq_ctx + S;     // [S + 1] exclusive bases of each sequence's slices
+  int *s_chk = s_dec + S + 1;  // [S + 1] ... and of its chunk units
+  int *s_pos = s_chk + S + 1;  // [S] first place of a decode sequence's slices, by size
+  __shared__ long long s_red[kPlanThreads / 32][2];
+  __shared__ int s_wd[kPlanThreads / 32], s_wc[kPlanThreads / 32];
+  __shared__ int s_hist[kSizeBuckets];
+  for (int b = tid; b < kSizeBuckets; b += kPlanThreads) s_hist[b] = 0;
 
-  // pass 1: decode pages, chunk KV tiles and chunk tile pairs of the step
-  long long pages = 0, tiles = 0, pairs = 0;
+  // pass 1: metadata, decode pages and chunk tile pairs of the step
+  long long pages = 0, pairs = 0;
   for (int s = tid; s < S; s += kPlanThreads) {
     const int qs = __ldg(p.query_start_loc + s);
     const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
-    if (q_len < 1) continue;
-    const int ctx = seq_ctx(p, s, q_len);
-    if (q_len == 1) {
-      pages += (long long)Hkv * ceil_div(ctx, kPage);
-    } else {
-      const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-      pairs += (long long)Hkv * npair;
-      long long t = 0;
-      for (int mp = 0; mp < npair; ++mp)
-        t += max(tile_kv<G>(ctx, q_len, 2 * mp), 2 * mp + 1 < mt ? tile_kv<G>(ctx, q_len, 2 * mp + 1) : 0);
-      tiles += t * Hkv;
-    }
+    const int ctx = q_len < 1 ? 0 : seq_ctx(p, s, q_len);
+    sq_qs[s] = qs;
+    sq_len[s] = q_len;
+    sq_ctx[s] = ctx;
+    if (q_len == 1) pages += (long long)Hkv * ceil_div(ctx, kPage);
+    else if (q_len > 1) pairs += (long long)Hkv * ((ceil_div(q_len * G, BM) + 1) / 2);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     pages += __shfl_xor_sync(0xffffffffu, pages, o);
-    tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
     pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
   }
-  if (lane == 0) { s_red[warp][0] = pages; s_red[warp][1] = tiles; s_red[warp][2] = pairs; }
+  if (lane == 0) { s_red[warp][0] = pages; s_red[warp][1] = pairs; }
   __syncthreads();
-  if (tid == 0) {
-    long long tp = 0, tt = 0, tq = 0;
-    for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tt += s_red[i][1]; tq += s_red[i][2]; }
-    const long long grid = w.grid;
-    // decode pages per slice: about two slices per CTA (every slice pays a
-    // pipeline fill and a finalisation; a segment cut into pieces also pays a
-    // merge), at least 16 pages
-    auto c8 = [](long long x) { return (x + 7) / 8 * 8; };
-    const long long P = max(16ll, c8((tp + 2 * grid - 1) / (2 * grid)));
-    // at most this many units per tile pair (only when the chunks have fewer
-    // tile pairs than CTAs; the split-unit partials hold kMaxStepGrid units)
-    const long long nu = (tq == 0 || tq >= grid) ? 1 : max(1ll, (long long)kMaxStepGrid / tq);
-    s_par[0] = (int)P;
-    s_par[1] = (int)nu;
-    (void)tt;
-  }
-  __syncthreads();
-  const int P = s_par[0], nu = s_par[1];
+  long long tp = 0, tq = 0;
+  for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tq += s_red[i][1]; }
+  const long long grid = w.grid;
+  // decode pages per slice: about one slice per CTA, so most segments stay
+  // whole (every slice pays a pipeline fill and a finalisation; a segment cut
+  // into pieces also pays a merge) while the longest-first order keeps the
+  // tail short; at least 16 pages, a multiple of the 8-page block
+  const int P = (int)max(16ll, ((tp + grid - 1) / grid + 7) / 8 * 8);
+  // at most this many units per tile pair (only when the chunks have fewer
+  // tile pairs than CTAs; the split-unit partials hold kMaxStepGrid units)
+  const int nu = (tq == 0 || tq >= grid) ? 1 : (int)max(1ll, (long long)kMaxStepGrid / tq);
+  auto units = [&](int s) {  // chunk units of one kv head of sequence s
+    const int mt = ceil_div(sq_len[s] * G, BM), npair = (mt + 1) / 2;
+    return npair * min(nu, ceil_div(tile_kv<G>(sq_ctx[s], sq_len[s], mt - 1), kUnitTiles));
+  };
+  auto pieces = [&](int s) { return ceil_div(ceil_div(sq_ctx[s], kPage), P); };
+  auto bucket = [&](int s) {  // size class of a decode sequence's pieces, in blocks
+    const int n = ceil_div(sq_ctx[s], kPage);
+    return min(ceil_div(ceil_div(n, pieces(s)), 8), kSizeBuckets - 1);
+  };
 
-  // pass 2: per-sequence counts, block exclusive scan over contiguous ranges
+  // pass 2: per-sequence counts, block exclusive scan over contiguous ranges;
+  // slice counts per size bucket
   const int per = ceil_div(S, kPlanThreads);
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
   int cd = 0, cc = 0;
   for (int s = s0; s < s1; ++s) {
-    const int qs = __ldg(p.query_start_loc + s);
-    const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
-    if (q_len < 1) continue;
-    const int ctx = seq_ctx(p, s, q_len);
-    if (q_len == 1) {
-      cd += Hkv * ceil_div(ceil_div(ctx, kPage), P);
-    } else {
-      const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-      const int nkv_max = tile_kv<G>(ctx, q_len, mt - 1);
-      cc += Hkv * npair * min(nu, ceil_div(nkv_max, kUnitTiles));
+    if (sq_len[s] == 1) {
+      const int n = Hkv * pieces(s);
+      cd += n;
+      atomicAdd(&s_hist[bucket(s)], n);
+    } else if (sq_len[s] > 1) {
+      cc += Hkv * units(s);
     }
   }
   int id = cd, ic = cc;
@@ -273,121 +278,92 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     const int a = __shfl_up_sync(0xffffffffu, id, o), b = __shfl_up_sync(0xffffffffu, ic, o);
     if (lane >= o) { id += a; ic += b; }
   }
-  __shared__ int s_wd[kPlanThreads / 32], s_wc[kPlanThreads / 32];
   if (lane == 31) { s_wd[warp] = id; s_wc[warp] = ic; }
   __syncthreads();
-  int bd = 0, bc = 0;
-  for (int i = 0; i < warp; ++i) { bd += s_wd[i]; bc += s_wc[i]; }
   {
-    int rd = bd + id - cd, rc = bc + ic - cc;
+    int rd = 0, rc = 0;
+    for (int i = 0; i < warp; ++i) { rd += s_wd[i]; rc += s_wc[i]; }
+    rd += id - cd;
+    rc += ic - cc;
     for (int s = s0; s < s1; ++s) {
       s_dec[s] = rd;
       s_chk[s] = rc;
-      const int qs = __ldg(p.query_start_loc + s);
-      const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
-      if (q_len < 1) continue;
-      const int ctx = seq_ctx(p, s, q_len);
-      if (q_len == 1) {
-        rd += Hkv * ceil_div(ceil_div(ctx, kPage), P);
-      } else {
-        const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-        const int nkv_max = tile_kv<G>(ctx, q_len, mt - 1);
-        rc += Hkv * npair * min(nu, ceil_div(nkv_max, kUnitTiles));
-      }
+      if (sq_len[s] == 1) rd += Hkv * pieces(s);
+      else if (sq_len[s] > 1) rc += Hkv * units(s);
     }
     if (tid == kPlanThreads - 1) { s_dec[S] = rd; s_chk[S] = rc; }
   }
+  // bucket bases from the largest size down (one bucket per thread)
+  static_assert(kSizeBuckets == kPlanThreads, "one size bucket per plan thread");
+  const int hb = kSizeBuckets - 1 - tid;  // thread 0 holds the largest bucket
+  const int hc = s_hist[hb];
+  int hi = hc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, hi, o);
+    if (lane >= o) hi += v;
+  }
+  __syncthreads();  // s_wd of pass 2 read; s_dec, s_chk complete
+  if (lane == 31) s_wd[warp] = hi;
+  __syncthreads();
+  {
+    int base = 0;
+    for (int i = 0; i < warp; ++i) base += s_wd[i];
+    s_hist[hb] = base + hi - hc;
+  }
+  __syncthreads();
+  // each decode sequence takes the next places of its bucket
+  for (int s = tid; s < S; s += kPlanThreads)
+    if (sq_len[s] == 1) s_pos[s] = atomicAdd(&s_hist[bucket(s)], Hkv * pieces(s));
   __syncthreads();
   const int Nd = s_dec[S], Nc = s_chk[S];
+  auto search = [&](const int *base, int k) {  // last s with base[s] <= k
+    int lo = 0, hi2 = S - 1;
+    while (lo < hi2) {
+      const int mid = (lo + hi2 + 1) >> 1;
+      if (base[mid] <= k) lo = mid; else hi2 = mid - 1;
+    }
+    return lo;
+  };
   // Queue order, longest items first: the chunk units (tile pairs from the
   // last, which see the most keys), then the decode slices by size.  The
   // dynamic queue then fills the SMs the chunk units leave free with decode
   // slices from the start, and ends on the shortest slices.
-  auto search = [&](const int *base, int k) {  // last s with base[s] <= k
-    int lo = 0, hi = S - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (base[mid] <= k) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
+  ItemDesc *list = reinterpret_cast<ItemDesc *>(w.list);
   for (int k = tid; k < Nc; k += kPlanThreads) {
     const int s = search(s_chk, k);
-    const int qs = __ldg(p.query_start_loc + s);
-    const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
-    const int ctx = seq_ctx(p, s, q_len);
+    const int q_len = sq_len[s];
     const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
-    const int nus = min(nu, ceil_div(tile_kv<G>(ctx, q_len, mt - 1), kUnitTiles));
+    const int nus = units(s) / npair;
     const int local = k - s_chk[s];
     const int pair = local / nus, u = local - pair * nus;
     const int mp = npair - 1 - pair / Hkv, g = pair % Hkv;  // later tiles (more keys) first
     ItemDesc d;
     d.s_kind = s;
-    d.qs = qs;
-    d.ctx = ctx;
+    d.qs = sq_qs[s];
+    d.ctx = sq_ctx[s];
     d.q_len = q_len;
     d.g_x = g | (mp << 8);
     d.a = u | (nus << 16);
     d.b = k;
     d.c = k - u;
-    reinterpret_cast<ItemDesc *>(w.list)[k] = d;
+    list[k] = d;
   }
-  // decode slices, longest first: histogram of their 8-page blocks, bases
-  // in descending order, then each slice takes the next place of its bucket
-  __shared__ int s_hist[kSizeBuckets];
-  for (int b = tid; b < kSizeBuckets; b += kPlanThreads) s_hist[b] = 0;
-  __syncthreads();
-  auto slice_geom = [&](int i, int &s, int &g, int &piece, int &p0, int &p1, int &ks, int &ctx) {
-    s = search(s_dec, i);
-    ctx = seq_ctx(p, s, 1);
-    const int n = ceil_div(ctx, kPage);
-    ks = ceil_div(n, P);
+  for (int i = tid; i < Nd; i += kPlanThreads) {
+    const int s = search(s_dec, i);
+    const int n = ceil_div(sq_ctx[s], kPage), ks = pieces(s);
     const int local = i - s_dec[s];
-    g = local / ks;
-    piece = local - g * ks;
-    p0 = (int)((long long)piece * n / ks);
-    p1 = (int)((long long)(piece + 1) * n / ks);
-  };
-  auto bucket = [&](int p0, int p1) { return min(ceil_div(p1 - p0, 8), kSizeBuckets - 1); };
-  for (int i = tid; i < Nd; i += kPlanThreads) {
-    int s, g, piece, p0, p1, ks, ctx;
-    slice_geom(i, s, g, piece, p0, p1, ks, ctx);
-    atomicAdd(&s_hist[bucket(p0, p1)], 1);
-  }
-  __syncthreads();
-  {
-    // exclusive scan from the largest bucket down (one bucket per thread)
-    static_assert(kSizeBuckets == kPlanThreads, "one size bucket per plan thread");
-    const int b = kSizeBuckets - 1 - tid;  // thread 0 takes the largest bucket
-    const int c = s_hist[b];
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_wd[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int i = 0; i < warp; ++i) base += s_wd[i];
-    __syncthreads();
-    s_hist[b] = base + incl - c;
-  }
-  __syncthreads();
-  for (int i = tid; i < Nd; i += kPlanThreads) {
-    int s, g, piece, p0, p1, ks, ctx;
-    slice_geom(i, s, g, piece, p0, p1, ks, ctx);
-    const int r = atomicAdd(&s_hist[bucket(p0, p1)], 1);  // place in the decode order
+    const int g = local / ks, piece = local - g * ks;
     ItemDesc d;
     d.s_kind = s | (KIND_DECODE << 30);
-    d.qs = __ldg(p.query_start_loc + s);
-    d.ctx = ctx;
+    d.qs = sq_qs[s];
+    d.ctx = sq_ctx[s];
     d.q_len = ks;
     d.g_x = g | (piece << 8);
-    d.a = p0;
-    d.b = p1;
+    d.a = (int)((long long)piece * n / ks);
+    d.b = (int)((long long)(piece + 1) * n / ks);
     d.c = i;  // partial slot: the slice's own index, whatever its place
-    reinterpret_cast<ItemDesc *>(w.list)[Nc + r] = d;
+    list[Nc + s_pos[s] + local] = d;
   }
   // merge counters of this step start at zero; so does the queue ticket
   for (int x = tid; x < S * Hkv; x += kPlanThreads) w.dec_ctr[x] = 0u;
@@ -1487,7 +1463,15 @@ cudaError_t launch_dg(const AttnParams &p, const StepWs &w, cudaStream_t stream)
     const int64_t pieces = (int64_t)p.num_tokens * p.Hkv * (D * 2 / 16);
     append_ctas = (int)std::min<int64_t>(w.grid, (pieces + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
   }
-  attn_plan_kernel<G><<<1 + append_ctas, kPlanThreads, 0, stream>>>(p, w);
+  static bool plan_configured = false;
+  if (!plan_configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_plan_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)plan_smem_bytes(kDecodeMaxSeqs));
+    if (e != cudaSuccess) return e;
+    plan_configured = true;
+  }
+  attn_plan_kernel<G><<<1 + append_ctas, kPlanThreads, plan_smem_bytes(p.num_seqs), stream>>>(p, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // ... then the step, allowed to start while the plan finishes
