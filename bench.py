@@ -285,23 +285,13 @@ def run_gpu(args, world, rank, local):
         step()
     torch.cuda.synchronize()
     # this library's kernels per step, as cpa_append_attention_forward
-    # dispatches them: the chunk-tile kernel (bf16, head_dim 64/128, GQA
-    # 1/2/4/8) when the step has chunks, the streaming decode kernel (bf16,
-    # GQA 2/4/8, group * head_dim <= 512) whenever that path applies, the row
-    # kernel for whatever neither takes, and a separate append launch unless
-    # the append is fused into the decode and chunk kernels
+    # dispatches them: on the step path (bf16, head_dim 64/128, GQA group
+    # 1/2/4/8) the plan kernel (which also does the append) and the persistent
+    # step kernel; otherwise the append and the row kernel
     G = sh.num_q_heads // sh.num_kv_heads
-    bf16 = sh.dtype == torch.bfloat16 and sh.head_dim in (64, 128)
-    fast_decode = bf16 and G in (2, 4, 8) and G * sh.head_dim <= 512
-    all_decode = all(q == 1 for q in m.q_lens)
-    launch_chunks = bf16 and G in (1, 2, 4, 8) and not all_decode
-    if launch_chunks and fast_decode:
-        attn_launches = 2
-    else:
-        rows = (not fast_decode) or (not all_decode and not launch_chunks)
-        attn_launches = int(fast_decode) + int(launch_chunks) + int(rows)
-    fused = fast_decode and (all_decode or launch_chunks)
-    launches_per_step = attn_launches + (0 if fused else 1)
+    step_path = sh.dtype == torch.bfloat16 and sh.head_dim in (64, 128) and G in (1, 2, 4, 8)
+    fused = step_path
+    launches_per_step = 2
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier(world)
@@ -434,8 +424,9 @@ def run_gpu(args, world, rank, local):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["kernel"] = ("append fused into attention (cpa_append_attention_forward)" if fused
-                      else "append + attention (cpa_append_attention_forward)")
+    roof["kernel"] = ("plan (with the append) + persistent step kernel "
+                      "(cpa_append_attention_forward)" if fused
+                      else "append + row attention (cpa_append_attention_forward)")
     roof["kernel_us"] = call_ms * 1e3
     roof["algorithmic_bytes"] = call_bytes
     roof["algorithmic_flops"] = counts["flops"]

@@ -66,9 +66,9 @@ constexpr int kDecN = 16;        // N of the decode MMAs: the G query rows, padd
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kPlanThreads = 1024;
 // A tile pair's KV range is split over several units only into pieces of at
-// least this many KV tiles (8192 keys): each unit pays a query load, a
-// pipeline fill and a partial-result merge.
-constexpr int kUnitTiles = 64;
+// least this many KV tiles: each unit pays a query load, a pipeline fill and
+// a partial-result merge.
+constexpr int kMinUnitTiles = 8;
 // Decode slices are queued longest first, bucketed by their 8-page blocks.
 constexpr int kSizeBuckets = 1024;
 
@@ -213,13 +213,13 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   int *s_dec = sq_ctx + S;     // [S + 1] exclusive bases of each sequence's slices
   int *s_chk = s_dec + S + 1;  // [S + 1] ... and of its chunk units
   int *s_pos = s_chk + S + 1;  // [S] first place of a decode sequence's slices, by size
-  __shared__ long long s_red[kPlanThreads / 32][2];
+  __shared__ long long s_red[kPlanThreads / 32][3];
   __shared__ int s_wd[kPlanThreads / 32], s_wc[kPlanThreads / 32];
   __shared__ int s_hist[kSizeBuckets];
   for (int b = tid; b < kSizeBuckets; b += kPlanThreads) s_hist[b] = 0;
 
-  // pass 1: metadata, decode pages and chunk tile pairs of the step
-  long long pages = 0, pairs = 0;
+  // pass 1: metadata, decode pages, chunk tile pairs and their KV tiles
+  long long pages = 0, pairs = 0, ctiles = 0;
   for (int s = tid; s < S; s += kPlanThreads) {
     const int qs = __ldg(p.query_start_loc + s);
     const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
@@ -227,30 +227,43 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     sq_qs[s] = qs;
     sq_len[s] = q_len;
     sq_ctx[s] = ctx;
-    if (q_len == 1) pages += (long long)Hkv * ceil_div(ctx, kPage);
-    else if (q_len > 1) pairs += (long long)Hkv * ((ceil_div(q_len * G, BM) + 1) / 2);
+    if (q_len == 1) {
+      pages += (long long)Hkv * ceil_div(ctx, kPage);
+    } else if (q_len > 1) {
+      const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
+      pairs += (long long)Hkv * npair;
+      // tiles per pair grow about linearly from the first pair to the last
+      ctiles += (long long)Hkv * npair * (tile_kv<G>(ctx, q_len, 1) + tile_kv<G>(ctx, q_len, mt - 1)) / 2;
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     pages += __shfl_xor_sync(0xffffffffu, pages, o);
     pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+    ctiles += __shfl_xor_sync(0xffffffffu, ctiles, o);
   }
-  if (lane == 0) { s_red[warp][0] = pages; s_red[warp][1] = pairs; }
+  if (lane == 0) { s_red[warp][0] = pages; s_red[warp][1] = pairs; s_red[warp][2] = ctiles; }
   __syncthreads();
-  long long tp = 0, tq = 0;
-  for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tq += s_red[i][1]; }
+  long long tp = 0, tq = 0, tt = 0;
+  for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tq += s_red[i][1]; tt += s_red[i][2]; }
   const long long grid = w.grid;
   // decode pages per slice: about one slice per CTA, so most segments stay
   // whole (every slice pays a pipeline fill and a finalisation; a segment cut
   // into pieces also pays a merge) while the longest-first order keeps the
   // tail short; at least 16 pages, a multiple of the 8-page block
   const int P = (int)max(16ll, ((tp + grid - 1) / grid + 7) / 8 * 8);
-  // at most this many units per tile pair (only when the chunks have fewer
-  // tile pairs than CTAs; the split-unit partials hold kMaxStepGrid units)
+  // Chunk tile pairs are split over several units when they are fewer than
+  // the CTAs, so that no unit is longer than half of a CTA's share of the
+  // step's work: its chunk KV tiles and decode blocks (both 128-key blocks
+  // of attention) over the grid.  Without that, one long unit (a short chunk
+  // with a long cached prefix) would set the step's length on its own.
+  // At most kMaxStepGrid units in all (the split-unit partials hold that many).
   const int nu = (tq == 0 || tq >= grid) ? 1 : (int)max(1ll, (long long)kMaxStepGrid / tq);
+  const int unit_tiles =
+      (int)max((long long)kMinUnitTiles, ((tt + (tp + 7) / 8 + grid - 1) / grid + 1) / 2);
   auto units = [&](int s) {  // chunk units of one kv head of sequence s
     const int mt = ceil_div(sq_len[s] * G, BM), npair = (mt + 1) / 2;
-    return npair * min(nu, ceil_div(tile_kv<G>(sq_ctx[s], sq_len[s], mt - 1), kUnitTiles));
+    return npair * min(nu, ceil_div(tile_kv<G>(sq_ctx[s], sq_len[s], mt - 1), unit_tiles));
   };
   auto pieces = [&](int s) { return ceil_div(ceil_div(sq_ctx[s], kPage), P); };
   auto bucket = [&](int s) {  // size class of a decode sequence's pieces, in blocks
