@@ -40,7 +40,7 @@ WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
     w.part_ml = off;
     off = align_up(off + sizeof(float2) * rows, 256);
     w.total = off;
-    w.clear = w.part_o;  // header and counters
+    w.clear = 256;  // the status word; every call zeroes its counters itself
     return w;
   }
   // capacities for a persistent grid of up to kMaxStepGrid CTAs (one per SM)
@@ -223,6 +223,10 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
                          p.page_size, p.num_pages, eb, p.status, st) != cudaSuccess)
       return CPA_ERR_CUDA;
   }
+  // the split-merge counters start at zero in every call, whatever an earlier
+  // call (one that gave up a bounded wait, say) or the caller left there
+  if (cudaMemsetAsync(ws + w.counters, 0, w.part_o - w.counters, st) != cudaSuccess)
+    return CPA_ERR_CUDA;
   p.counters = reinterpret_cast<uint32_t *>(ws + w.counters);
   p.part_o = reinterpret_cast<float *>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);

@@ -65,10 +65,10 @@ extern "C" int cpa_attention_forward_noalloc(const void *q, const void *k_cache,
   if (!scratch) return CPA_ERR_CUDA;
   d.workspace = scratch;
   d.workspace_bytes = CPA_NOALLOC_SCRATCH_BYTES;
-  // The status word and the merge counters must start at zero; an earlier
-  // call left the array as it finished (or gave up).  They are cleared on the
-  // caller's stream only once the call has passed every check, right before
-  // its first launch.
+  // The status word starts at zero in every no-alloc call (the word reports
+  // this call only); the work queue and merge counters are reset by the call
+  // itself.  The clear runs on the caller's stream only once the call has
+  // passed every check, right before its first launch.
   const WorkspaceLayout w = workspace_layout(d, num_seqs);
   return attention(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, num_seqs,
                    scale, out, stream, &d, NewRows{}, w.clear);

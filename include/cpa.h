@@ -50,9 +50,24 @@ typedef enum {
   CPA_ERR_UNSUPPORTED = -2,  /* valid but not supported (e.g. head_dim 96)     */
   CPA_ERR_WORKSPACE = -3,    /* workspace missing, misaligned or too small     */
   CPA_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed           */
-  CPA_ERR_DEVICE = -5        /* a kernel found an out-of-range index (status
-                                word, read back with cpa_read_device_status)  */
+  CPA_ERR_DEVICE = -5        /* a kernel found an out-of-range index or gave
+                                up a bounded wait (status word, read back with
+                                cpa_read_device_status)                       */
 } cpa_status;
+
+/* After CPA_ERR_DEVICE.  The word collects, since its last read, bit 1: a
+ * block_table entry outside [0, num_pages) (that page was skipped), bit 2: a
+ * slot_mapping entry past the cache (that row was not written), bit 4: a
+ * bounded wait in the step kernel gave up (after 2^22 polls of its barrier,
+ * on the order of a second; the CTA drained its copies and left, so some output rows of that call were
+ * not written).  The output of every call since the last read is then
+ * unreliable and must be recomputed; the cache rows the calls appended are
+ * still valid unless bit 2 is set.  Nothing else needs resetting: the read
+ * clears the word, and the next call rebuilds its work queue and zeroes its
+ * counters itself.  Bits 1 and 2 mean the metadata is wrong; fix it before
+ * re-running.  Bit 4 alone means the GPU did not run the kernel's CTAs to
+ * completion in time (for instance a stream starved for longer than the wait
+ * limit by other work); the same call can simply be issued again. */
 
 typedef enum { CPA_F32 = 0, CPA_BF16 = 1 } cpa_dtype;
 
@@ -68,9 +83,11 @@ typedef struct cpa_desc {
   int32_t dtype;              /* cpa_dtype                                    */
   int64_t num_tokens;         /* packed tokens this step (query_start_loc[S]) */
   void *workspace;            /* device scratch, >= cpa_workspace_bytes(),
-                                 256-byte aligned, zero-filled before its first
-                                 use; every completed attention call leaves it
-                                 ready for the next one                       */
+                                 256-byte aligned.  Only its first 4 bytes (the
+                                 device status word) must be zero before the
+                                 first call; every call resets the rest of the
+                                 state it uses (work queue, merge counters),
+                                 whatever an earlier call left there          */
   size_t workspace_bytes;
 } cpa_desc;
 
@@ -82,7 +99,8 @@ const char *cpa_status_string(int status);
  * arithmetic; returns 0 if the description is invalid.  The workspace holds
  * the step's work queue, the split-KV partial results (o, running max, running
  * sum) of decode segments and of chunk tiles split over several CTAs, their
- * arrival counters (zeroed by every call before use), and a device status
+ * arrival counters (zeroed by every call before use, never carried over from
+ * an earlier call), and a device status
  * word.  It is sized for a GPU of up to 256 SMs. */
 size_t cpa_workspace_bytes(const cpa_desc *desc, int32_t num_seqs);
 
@@ -173,9 +191,9 @@ size_t cpa_noalloc_scratch_bytes(void);
  *    it before any stream capture.  CPA_ERR_CUDA if the lookup fails.
  *  - Sharing: every call on a device uses the same array, which keeps what the
  *    last call left in it.  Once a call has passed its argument checks it
- *    clears the array's status word (and the merge counters the call uses) on
- *    `stream`, right before its first launch; a rejected or empty call
- *    touches nothing.
+ *    clears the array's status word on `stream`, right before its first
+ *    launch (the call resets its work queue and merge counters itself); a
+ *    rejected or empty call touches nothing.
  *    Calls whose work overlaps on the GPU (different streams, or different
  *    host threads) race on the array: serialise them.
  *  - Errors: those of cpa_attention_forward; out-of-range indices met by the

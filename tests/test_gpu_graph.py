@@ -1,9 +1,10 @@
 """The step (append + attention) captured in a CUDA graph and replayed.
 
-The attention call forks the chunk tiles onto a side stream with events and
-joins them back, launches nothing that synchronises, and resets its split-merge
-counters itself, so a captured step replays to the same bits as the eager call
-on the same inputs -- and again on a second replay."""
+The attention call is two launches on the caller's stream (the plan kernel,
+then the persistent step kernel as its programmatic dependent), launches
+nothing that synchronises, and rebuilds its work queue and counters itself, so
+a captured step replays to the same bits as the eager call on the same inputs
+-- and again on a second replay."""
 import math
 
 import pytest
@@ -20,8 +21,8 @@ def bits(t):
 
 
 def test_captured_step_replays_bit_for_bit(cuda_device):
-    # two chunks (one with a cached prefix) beside four decodes: the chunk tiles
-    # run on the side stream next to the decode kernel
+    # two chunks (one with a cached prefix) beside four decodes: chunk tiles and
+    # decode slices share the step kernel's work queue
     q_lens = [33, 1, 129, 1, 1, 1]
     seq_lens = [50, 1100, 429, 3, 700, 2000]
     Hq, Hkv, D = 32, 8, 128

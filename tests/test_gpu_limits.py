@@ -1,8 +1,8 @@
 """Edges of the supported sizes, on the GPU.
 
-The streaming decode kernel holds one page-stream offset per sequence in
-shared memory, up to 4096 sequences per call; a larger batch is refused on the
-host (CPA_ERR_UNSUPPORTED) before anything is launched.  The largest batch is
+The plan kernel holds each sequence's metadata (lengths, item counts, queue
+offsets) in shared memory, up to 4096 sequences per call; a larger batch is
+refused on the host (CPA_ERR_UNSUPPORTED) before anything is launched.  The largest batch is
 checked against the oracle through both the separate calls and the fused
 append + attention call."""
 import math
