@@ -34,8 +34,14 @@
  * each [num_pages][Hkv][page_size][D].  Logical position j of sequence s lives
  * in page block_table[s][j / page_size] at offset j % page_size.
  *
- * Inputs are the exact stored values (fp32, or bf16 bit patterns), widened to
- * double.  All arithmetic is in double.
+ * Inputs are the exact stored values widened to double: fp32, bf16 or IEEE
+ * binary16 queries and caches, or an 8-bit cache of OCP FP8 E4M3 codes whose
+ * values are multiplied by a per-tensor scale (k_scale for K, v_scale for V).
+ * The pages do not cover an 8-bit cache; the format, its rounding and the
+ * scale follow the OCP 8-bit Floating Point Specification (OFP8), E4M3: 1 sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits, subnormals at exponent
+ * field 0, no infinities, S.1111.111 the only NaN, largest finite 448.
+ * All arithmetic is in double.
  */
 #include <math.h>
 #include <pthread.h>
@@ -43,16 +49,63 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2, ORACLE_E4M3 = 3 };
 
-/* One stored element widened to double.  bf16 is the upper half of an IEEE
- * binary32, so the widening is exact. */
+/* IEEE 754 binary16: sign, 5-bit exponent with bias 15, 10-bit fraction;
+ * exponent field 0 holds zero and the subnormals (fraction * 2^-24), 31 the
+ * infinities and NaNs. */
+static double f16_value(uint16_t h) {
+  int sign = h >> 15, ef = (h >> 10) & 31, fr = h & 1023;
+  double v;
+  if (ef == 31) v = fr ? NAN : INFINITY;
+  else if (ef == 0) v = ldexp((double)fr, -24);
+  else v = ldexp((double)(1024 + fr), ef - 25);
+  return sign ? -v : v;
+}
+
+/* OFP8 E4M3: exponent field 0 holds zero and the subnormals (mantissa * 2^-9);
+ * otherwise (8 + mantissa) * 2^(exponent field - 10); S.1111.111 is NaN. */
+static double e4m3_value(uint8_t b) {
+  int sign = b >> 7, ef = (b >> 3) & 15, m = b & 7;
+  if (ef == 15 && m == 7) return NAN;
+  double v = ef == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), ef - 10);
+  return sign ? -v : v;
+}
+
+/* One stored element widened to double (exact for every format here).  bf16
+ * is the upper half of an IEEE binary32. */
 static double load_elem(const void *base, int dtype, int64_t idx) {
   if (dtype == ORACLE_F32) return (double)((const float *)base)[idx];
+  if (dtype == ORACLE_F16) return f16_value(((const uint16_t *)base)[idx]);
+  if (dtype == ORACLE_E4M3) return e4m3_value(((const uint8_t *)base)[idx]);
   uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
+}
+
+/* OFP8 E4M3 code of a binary32 value: round to nearest, ties to even, at the
+ * spacing of the value's binade (the subnormal spacing 2^-9 below 2^-6), and
+ * saturate to +-448 (magnitudes that round past 448, and infinities); NaN
+ * gives the NaN code 0x7f.  With e = max(floor(log2|y|), -6) and
+ * m = |y| / 2^(e-3) rounded to an integer, the code is 8 (e + 6) + m: this
+ * covers subnormals (e = -6, m < 8) and a mantissa that rounds up into the
+ * next binade (m = 16) alike. */
+static uint8_t e4m3_code(float y) {
+  if (isnan(y)) return 0x7f;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a >= 448.0) return sign | 0x7e;
+  int e = -6;
+  if (a > 0.0) {
+    int ex;
+    frexp(a, &ex);  /* a = f * 2^ex, 0.5 <= f < 1 */
+    if (ex - 1 > e) e = ex - 1;
+  }
+  double m = nearbyint(a / ldexp(1.0, e - 3));  /* exact quotient; ties to even */
+  int code = 8 * (e + 6) + (int)m;
+  if (code > 0x7e) code = 0x7e;
+  return sign | (uint8_t)code;
 }
 
 /* Element offset of (logical position j, kv head g, dim 0) of sequence s. */
@@ -65,7 +118,9 @@ static int64_t cache_offset(const int32_t *block_table, int max_pages, int s,
 
 typedef struct {
   const void *q, *k_cache, *v_cache;
-  int dtype;
+  int dtype;     /* element type of q */
+  int kv_dtype;  /* element type of the caches */
+  double k_scale, v_scale;  /* cache values are stored values times these */
   const int32_t *block_table;
   int max_pages;
   const int32_t *query_start_loc, *seq_lens;
@@ -105,7 +160,8 @@ static int64_t attend_one(const oracle_problem *P, int64_t t, int h,
     double dot = 0.0;
     for (int d = 0; d < D; ++d)
       dot += load_elem(P->q, P->dtype, q_base + d) *
-             load_elem(P->k_cache, P->dtype, kb + d);
+             load_elem(P->k_cache, P->kv_dtype, kb + d);
+    dot *= P->k_scale;                         /* K = k_scale * stored K */
     x[j] = P->scale * dot;
     if (x[j] > mx) mx = x[j];
   }
@@ -120,7 +176,8 @@ static int64_t attend_one(const oracle_problem *P, int64_t t, int h,
     if (probs) probs[j] = p;
     int64_t vb = cache_offset(P->block_table, P->max_pages, s, j, g, P->Hkv, D,
                               P->page_size);
-    for (int d = 0; d < D; ++d) out[d] += p * load_elem(P->v_cache, P->dtype, vb + d);
+    for (int d = 0; d < D; ++d)
+      out[d] += p * (P->v_scale * load_elem(P->v_cache, P->kv_dtype, vb + d));
   }
   return n_vis;
 }
@@ -149,19 +206,22 @@ static void *run_job(void *arg) {
   return NULL;
 }
 
-/* Attention output for the packed query tokens listed in rows[0..num_rows).
- * out is [num_rows][Hq][D] doubles.  nthreads >= 1 workers split the rows.
- * Returns 0, or -1 on malformed metadata, -2 on allocation failure. */
-int oracle_attention(const void *q, const void *k_cache, const void *v_cache,
-                     int dtype, const int32_t *block_table, int max_pages,
-                     const int32_t *query_start_loc, const int32_t *seq_lens,
-                     int num_seqs, int Hq, int Hkv, int D, int page_size,
-                     double scale, const int64_t *rows, int64_t num_rows,
-                     double *out, int nthreads) {
+/* Attention output for the packed query tokens listed in rows[0..num_rows),
+ * q of element type q_dtype, caches of element type kv_dtype holding
+ * K / k_scale and V / v_scale.  out is [num_rows][Hq][D] doubles.
+ * nthreads >= 1 workers split the rows.  Returns 0, or -1 on malformed
+ * metadata, -2 on allocation failure. */
+int oracle_attention_kv(const void *q, int q_dtype, const void *k_cache,
+                        const void *v_cache, int kv_dtype, double k_scale,
+                        double v_scale, const int32_t *block_table, int max_pages,
+                        const int32_t *query_start_loc, const int32_t *seq_lens,
+                        int num_seqs, int Hq, int Hkv, int D, int page_size,
+                        double scale, const int64_t *rows, int64_t num_rows,
+                        double *out, int nthreads) {
   if (Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0 || D <= 0) return -1;
-  oracle_problem P = {q, k_cache, v_cache, dtype, block_table, max_pages,
-                      query_start_loc, seq_lens, num_seqs, Hq, Hkv, D,
-                      page_size, scale};
+  oracle_problem P = {q, k_cache, v_cache, q_dtype, kv_dtype, k_scale, v_scale,
+                      block_table, max_pages, query_start_loc, seq_lens,
+                      num_seqs, Hq, Hkv, D, page_size, scale};
   int64_t max_ctx = 0;
   for (int s = 0; s < num_seqs; ++s)
     if (seq_lens[s] > max_ctx) max_ctx = seq_lens[s];
@@ -187,6 +247,19 @@ int oracle_attention(const void *q, const void *k_cache, const void *v_cache,
   return status;
 }
 
+/* The same with q and caches of one element type and unit scales. */
+int oracle_attention(const void *q, const void *k_cache, const void *v_cache,
+                     int dtype, const int32_t *block_table, int max_pages,
+                     const int32_t *query_start_loc, const int32_t *seq_lens,
+                     int num_seqs, int Hq, int Hkv, int D, int page_size,
+                     double scale, const int64_t *rows, int64_t num_rows,
+                     double *out, int nthreads) {
+  return oracle_attention_kv(q, dtype, k_cache, v_cache, dtype, 1.0, 1.0,
+                             block_table, max_pages, query_start_loc, seq_lens,
+                             num_seqs, Hq, Hkv, D, page_size, scale, rows,
+                             num_rows, out, nthreads);
+}
+
 /* Softmax weights of one (packed token t, head h) over its visible keys.
  * probs must hold seq_lens[s] doubles; out holds D doubles.  Returns the
  * number of visible keys, or a negative status. */
@@ -196,9 +269,9 @@ int64_t oracle_probs(const void *q, const void *k_cache, const void *v_cache,
                      int num_seqs, int Hq, int Hkv, int D, int page_size,
                      double scale, int64_t t, int h, double *probs, double *out) {
   if (Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0 || D <= 0) return -1;
-  oracle_problem P = {q, k_cache, v_cache, dtype, block_table, max_pages,
-                      query_start_loc, seq_lens, num_seqs, Hq, Hkv, D,
-                      page_size, scale};
+  oracle_problem P = {q, k_cache, v_cache, dtype, dtype, 1.0, 1.0, block_table,
+                      max_pages, query_start_loc, seq_lens, num_seqs, Hq, Hkv,
+                      D, page_size, scale};
   int s = owner_seq(&P, t);
   if (s < 0) return -1;
   double *scratch = (double *)malloc(sizeof(double) * (size_t)(seq_lens[s] + 1));
@@ -226,6 +299,48 @@ void oracle_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
       size_t src = (size_t)(t * Hkv + g) * row;
       memcpy((char *)k_cache + dst, (const char *)k + src, row);
       memcpy((char *)v_cache + dst, (const char *)v + src, row);
+    }
+  }
+}
+
+/* E4M3 codes of x[0..n) / scale, the quotient taken in binary32 (one
+ * correctly rounded division), x of element type dtype. */
+void oracle_e4m3_encode(const void *x, int dtype, int64_t n, float scale,
+                        uint8_t *out) {
+  for (int64_t i = 0; i < n; ++i) {
+    float xi = (float)load_elem(x, dtype, i);  /* exact: every input type fits */
+    float y = xi / scale;
+    out[i] = e4m3_code(y);
+  }
+}
+
+/* Values of E4M3 codes. */
+void oracle_e4m3_decode(const uint8_t *codes, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+}
+
+/* Values of IEEE binary16 bit patterns. */
+void oracle_f16_decode(const uint16_t *bits, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f16_value(bits[i]);
+}
+
+/* KV append into an E4M3 cache: token t's K row (all kv heads) is stored as
+ * the codes of k / k_scale at slot_mapping[t], V likewise with v_scale; a
+ * negative slot means "no cache write".  k and v have element type dtype. */
+void oracle_kv_append_e4m3(const void *k, const void *v, int dtype,
+                           const int64_t *slot_mapping, int64_t num_tokens,
+                           int Hkv, int D, int page_size, float k_scale,
+                           float v_scale, uint8_t *k_cache, uint8_t *v_cache) {
+  int eb = dtype == ORACLE_F32 ? 4 : 2;
+  for (int64_t t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    int64_t page = slot / page_size, off = slot % page_size;
+    for (int g = 0; g < Hkv; ++g) {
+      int64_t dst = ((page * Hkv + g) * page_size + off) * (int64_t)D;
+      int64_t src = (t * Hkv + g) * (int64_t)D;
+      oracle_e4m3_encode((const char *)k + src * eb, dtype, D, k_scale, k_cache + dst);
+      oracle_e4m3_encode((const char *)v + src * eb, dtype, D, v_scale, v_cache + dst);
     }
   }
 }
