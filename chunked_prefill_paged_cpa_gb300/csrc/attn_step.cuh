@@ -45,6 +45,19 @@
 //              maximum (and with it the accumulator) moves only when it grew
 //              by more than 2^8.  Decode pipelines take alternate blocks of a
 //              slice and merge at its end through TMEM.
+//
+// Cache modes (template KVM): 0 bf16 queries and cache; 1 binary16 queries
+// and cache; 2 a cache of OCP FP8 E4M3 codes.  In mode 2 each page of codes
+// lands in the upper half of its page's 16-bit destination in the K/V stage,
+// and the eight softmax warps widen it in place to binary16 (exact), one page
+// per warp, every fill in the producer's order, before the MMAs read it; the
+// MMAs then take binary16 operands (queries converted to binary16 by the plan
+// kernel when they are bf16), k_scale is folded into the softmax scale and
+// v_scale into the output.  The widening also zeroes the rows of cache slots
+// past the sequence.
+//
+// This header is compiled once per cache mode (attn_step_<mode>.cu).
+#pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -94,6 +107,13 @@ struct StepCfg {
   // The decode PV uses M = 128 rows of V^T; at head_dim 64 its upper half reads
   // the next 2 KB (never used): keep that inside the allocation.
   static constexpr int PAD = D == 64 ? 2048 : 0;
+  // E4M3 cache: where a page of codes (16 rows x D bytes) lands inside the
+  // 16-bit stage, within page i's own destination: K at K8_OFF + i * 2 KB
+  // (the last panel's slot of the page at D = 128, the slot's second half at
+  // D = 64), V at V8_OFF + i * PAGE_BYTES (the page's second half)
+  static constexpr int PAGE8 = 16 * D;
+  static constexpr int K8_OFF = D == 128 ? BN * 128 : 1024;
+  static constexpr int V8_OFF = PAGE_BYTES / 2;
   static constexpr int OFF_BAR = OFF_V + VST * KV_BYTES + PAD;
   static constexpr int BAR_BYTES = 2048;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // barriers and scratch, 1 KB alignment
@@ -116,6 +136,7 @@ struct WorkItem {
 struct Bars {
   uint64_t q_full[2], q_empty[2], k_full[3], k_empty[3], v_full[3], v_empty[3], s_full[2],
       p_full[2], o_final[2];
+  uint64_t k_conv[3], v_conv[3];  // E4M3 cache: a fill widened (256 arrivals)
   uint64_t item_full[kItemSlots], item_empty[kItemSlots];
   uint64_t wg_bar[2];            // softmax warpgroup syncs (128 arrivals)
   uint64_t hand_off, release;    // decode pipelines' merge (128 arrivals each)
@@ -168,7 +189,18 @@ struct ItemDesc {
 // length, context, two exclusive bases and a queue place
 inline size_t plan_smem_bytes(int num_seqs) { return sizeof(int) * (6 * (size_t)num_seqs + 2); }
 
-template <int G>
+// 16-byte pieces of the plan's side work: the fused append's rows, then (E4M3
+// cache with bf16 queries) the queries to convert to binary16.
+template <int KVM>
+__host__ __device__ __forceinline__ int64_t plan_append_pieces(const AttnParams &p) {
+  return p.fused ? (int64_t)p.num_tokens * p.Hkv * (p.D * 2 / 16) : 0;
+}
+template <int KVM>
+__host__ __device__ __forceinline__ int64_t plan_q_pieces(const AttnParams &p) {
+  return (KVM == 2 && !p.act_f16) ? (int64_t)p.num_tokens * p.Hq * (p.D * 2 / 16) : 0;
+}
+
+template <int KVM, int G>
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParams p,
                                                                   const StepWs w) {
   // the step kernel may be scheduled now: it waits in grid_dependency_wait
@@ -176,16 +208,24 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   ptx::grid_launch_dependents();
   const int tid = threadIdx.x;
   if (blockIdx.x > 0) {
-    // the append: every new row into its cache slot, 16 bytes per thread
-    const int CPR = p.D * 2 / 16;  // 16-byte pieces per row
-    const int64_t total = (int64_t)p.num_tokens * p.Hkv * CPR;
+    // the append: every new row into its cache slot, 16 bytes of input per
+    // thread (an E4M3 cache stores their 8 codes); then the queries' binary16
+    // copy when the MMAs need one
+    const int CPR = p.D * 2 / 16;  // 16-byte pieces per input row
+    const int64_t na = plan_append_pieces<KVM>(p), total = na + plan_q_pieces<KVM>(p);
     const int64_t stride = (int64_t)(gridDim.x - 1) * blockDim.x;
     const int64_t num_slots = p.num_pages * kPage;
     const uint4 *kin = static_cast<const uint4 *>(p.k_new);
     const uint4 *vin = static_cast<const uint4 *>(p.v_new);
-    uint4 *kc = static_cast<uint4 *>(const_cast<void *>(p.k_cache));
-    uint4 *vc = static_cast<uint4 *>(const_cast<void *>(p.v_cache));
     for (int64_t i = (int64_t)(blockIdx.x - 1) * blockDim.x + tid; i < total; i += stride) {
+      if (i >= na) {
+        const uint4 x = __ldg(static_cast<const uint4 *>(p.q) + (i - na));
+        uint32_t in[4] = {x.x, x.y, x.z, x.w}, o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = ptx::pack_f16x2(bf16_lo(in[e]), bf16_hi(in[e]));
+        static_cast<uint4 *>(p.q16)[i - na] = make_uint4(o[0], o[1], o[2], o[3]);
+        continue;
+      }
       const int64_t row = i / CPR, t = row / p.Hkv;
       const int g = (int)(row - t * p.Hkv), ch = (int)(i - row * CPR);
       const int64_t sl = __ldg(p.slot_mapping + t);
@@ -194,8 +234,22 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
       } else if (sl >= 0) {
         const int64_t pg = sl / kPage, off = sl - pg * kPage;
         const int64_t dst = ((pg * p.Hkv + g) * kPage + off) * CPR + ch;
-        kc[dst] = __ldg(kin + i);
-        vc[dst] = __ldg(vin + i);
+        if (KVM == 2) {
+          uint2 *kc = static_cast<uint2 *>(const_cast<void *>(p.k_cache));
+          uint2 *vc = static_cast<uint2 *>(const_cast<void *>(p.v_cache));
+          if (p.act_f16) {
+            kc[dst] = ptx::quantise8_e4m3<true>(__ldg(kin + i), p.k_scale);
+            vc[dst] = ptx::quantise8_e4m3<true>(__ldg(vin + i), p.v_scale);
+          } else {
+            kc[dst] = ptx::quantise8_e4m3<false>(__ldg(kin + i), p.k_scale);
+            vc[dst] = ptx::quantise8_e4m3<false>(__ldg(vin + i), p.v_scale);
+          }
+        } else {
+          uint4 *kc = static_cast<uint4 *>(const_cast<void *>(p.k_cache));
+          uint4 *vc = static_cast<uint4 *>(const_cast<void *>(p.v_cache));
+          kc[dst] = __ldg(kin + i);
+          vc[dst] = __ldg(vin + i);
+        }
       }
     }
     ptx::fence_proxy_async_global();
@@ -400,8 +454,9 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&sr)[32], int n) {
     if (e >= n) sr[e] = __float_as_uint(-INFINITY);
 }
 
-// p = exp2(s * scale - m) for 32 columns as 16 bf16 pairs in `pw`; the fp32
-// row sum (packed pairs) goes to four independent accumulators.
+// p = exp2(s * scale - m) for 32 columns as 16 bf16 (F16: binary16) pairs in
+// `pw`; the fp32 row sum (packed pairs) goes to four independent accumulators.
+template <bool F16>
 __device__ __forceinline__ void exp_chunk_regs(const uint32_t (&sr)[32], uint64_t sc2, uint64_t nm2,
                                                uint64_t (&rs2)[4], uint32_t (&pw)[16]) {
 #pragma unroll
@@ -412,8 +467,68 @@ __device__ __forceinline__ void exp_chunk_regs(const uint32_t (&sr)[32], uint64_
     ptx::unpack2(x2, x0, x1);
     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
     rs2[h & 3] = ptx::fadd2(rs2[h & 3], ptx::pack2(p0, p1));
-    pw[h] = ptx::pack_bf16x2(p0, p1);
+    pw[h] = F16 ? ptx::pack_f16x2(p0, p1) : ptx::pack_bf16x2(p0, p1);
   }
+}
+
+// Output elements: bf16 or binary16 (mode 2: as the caller's dtype says).
+template <int KVM>
+__device__ __forceinline__ bool out_f16(const AttnParams &p) {
+  return KVM == 1 || (KVM == 2 && p.act_f16);
+}
+__device__ __forceinline__ uint32_t pack_out2(float a, float b, bool f16) {
+  return f16 ? ptx::pack_f16x2(a, b) : ptx::pack_bf16x2(a, b);
+}
+__device__ __forceinline__ uint16_t cvt_out(float a, bool f16) {
+  return f16 ? __half_as_ushort(__float2half_rn(a)) : __bfloat16_as_ushort(__float2bfloat16_rn(a));
+}
+
+// One page of E4M3 codes (16 rows x D bytes at `src`, row-major) widened to
+// binary16 in the 128-byte-swizzled layout the MMAs read: row rr of panel p at
+// dst + p * pstride + rr * 128, its 16-byte chunk c at position c ^ (rr & 7).
+// Rows >= zrow (cache slots past the sequence) become zeros.  The codes lie
+// inside the page's own destination (the last panel's rows at D = 128, the
+// second half of the rows at D = 64): taken a group of rows at a time, in
+// order, a group's stores land only on its own codes (read before the
+// __syncwarp) or on those of groups already done.
+template <int D>
+__device__ __forceinline__ void widen_page(const unsigned char *src, unsigned char *dst,
+                                           int pstride, int zrow, int lane) {
+  constexpr int CPR = D / 16;       // 16-byte chunks of codes per row
+  constexpr int N = 16 * CPR / 32;  // groups of 32 / CPR rows: 4 (D = 128) or 2 (D = 64)
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int c = lane + 32 * k, rr = c / CPR, cc = c % CPR;
+    const uint4 in = *reinterpret_cast<const uint4 *>(src + c * 16);
+    __syncwarp();
+    uint32_t w[8];
+    ptx::e4m3x4_to_f16x4(in.x, w[0], w[1]);
+    ptx::e4m3x4_to_f16x4(in.y, w[2], w[3]);
+    ptx::e4m3x4_to_f16x4(in.z, w[4], w[5]);
+    ptx::e4m3x4_to_f16x4(in.w, w[6], w[7]);
+    if (rr >= zrow) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = 0u;
+    }
+    const uint4 lo = make_uint4(w[0], w[1], w[2], w[3]), hi = make_uint4(w[4], w[5], w[6], w[7]);
+    const int panel = cc >> 2, s = rr & 7;
+    unsigned char *row = dst + panel * pstride + rr * 128;
+    // dims 16 cc .. 16 cc + 15 are chunks 2 (cc & 3) and 2 (cc & 3) + 1 of the
+    // panel row; lanes of odd panels store their second chunk first, so each
+    // quarter warp's stores cover all eight bank groups
+    const int odd = panel & 1, j0 = 2 * (cc & 3) + odd;
+    *reinterpret_cast<uint4 *>(row + ((j0 ^ s) << 4)) = odd ? hi : lo;
+    *reinterpret_cast<uint4 *>(row + (((j0 ^ 1) ^ s) << 4)) = odd ? lo : hi;
+  }
+}
+
+// Which fill of an item the producer issues f-th (K_0, K_1, V_0, K_2, V_1, ...,
+// K_{n-1}, V_{n-2}, V_{n-1}): sets is_v and the tile.
+__device__ __forceinline__ void fill_of(int f, int n, bool &is_v, int &t) {
+  if (f == 0) { is_v = false; t = 0; }
+  else if (f == 2 * n - 1) { is_v = true; t = n - 1; }
+  else if (f & 1) { is_v = false; t = (f + 1) >> 1; }
+  else { is_v = true; t = (f - 2) >> 1; }
 }
 
 // Derive an item's geometry from its queue entry (every lane computes the same).
@@ -506,7 +621,7 @@ struct VRing {
   }
 };
 
-template <int D, int G>
+template <int KVM, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUtensorMap tm_q,
                  const __grid_constant__ CUtensorMap tm_qd, const __grid_constant__ CUtensorMap tm_k,
@@ -531,6 +646,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       ptx::mbar_init(&bs->k_empty[i], 2);
       ptx::mbar_init(&bs->v_full[i], 1);
       ptx::mbar_init(&bs->v_empty[i], 2);
+      ptx::mbar_init(&bs->k_conv[i], 256);
+      ptx::mbar_init(&bs->v_conv[i], 256);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&bs->q_full[i], 1);
@@ -684,7 +801,16 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         int rows[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rows[i] = __shfl_sync(0xffffffffu, src, (t & 3) * 8 + i);
-        if (lane == 0) {
+        if (KVM == 2) {
+          // pages of E4M3 codes into the upper half of each page's destination
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar, 8 * C::PAGE8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              ptx::tma_load_2d(dst + (is_v ? i * C::PAGE_BYTES + C::V8_OFF : i * kPage * 128 + C::K8_OFF),
+                               is_v ? &tm_v : &tm_k, 0, rows[i], bar);
+          }
+        } else if (lane == 0) {
           ptx::mbar_arrive_expect_tx(bar, C::KV_BYTES);
           if (is_v) {
 #pragma unroll
@@ -757,10 +883,15 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       return false;
     };
     auto unlock = [&]() { atomicExch(&bs->mma_lock, 0u); };
-    constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
-    constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
-    constexpr uint32_t idesc_qk_d = ptx::idesc_bf16_f32(BN, kDecN, false, false);
-    constexpr uint32_t idesc_pv_d = ptx::idesc_bf16_f32(128, kDecN, true, false);
+    constexpr bool F16 = KVM != 0;  // binary16 operands
+    constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false, F16);
+    constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true, F16);
+    constexpr uint32_t idesc_qk_d = ptx::idesc_bf16_f32(BN, kDecN, false, false, F16);
+    constexpr uint32_t idesc_pv_d = ptx::idesc_bf16_f32(128, kDecN, true, false, F16);
+    // a K/V fill is ready for the MMAs once it has landed, or, for an E4M3
+    // cache, once the softmax warps have widened it
+    uint64_t *const kready = KVM == 2 ? bs->k_conv : bs->k_full;
+    uint64_t *const vready = KVM == 2 ? bs->v_conv : bs->v_full;
     const uint32_t tS = tmem + ti * 128, tO = tmem + 256 + ti * 128;
     constexpr int KS = D / 16, VS = BN / 16;
     uint64_t qdesc[KS], kdesc[C::KST][KS], vdesc[3][VS], qtdesc[2][KS], ptdesc[VS];
@@ -813,13 +944,13 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         // tiles may be read by one query tile only).
         auto ack_k1 = [&](int t) -> bool {  // observe K fill of tile t, release it
           const uint32_t kc = kvm + t;
-          if (!ptx::mbar_wait(&bs->k_full[kc % C::KST], (kc / C::KST) & 1)) return false;
+          if (!ptx::mbar_wait(&kready[kc % C::KST], (kc / C::KST) & 1)) return false;
           ptx::mbar_arrive(&bs->k_empty[kc % C::KST]);
           return true;
         };
         auto ack_v1 = [&](int t) -> bool {  // observe V fill of tile t, release it
           const int st = vr.stage(t);
-          if (!ptx::mbar_wait(&bs->v_full[st], vr.use(t) & 1)) return false;
+          if (!ptx::mbar_wait(&vready[st], vr.use(t) & 1)) return false;
           ptx::mbar_arrive(&bs->v_empty[st]);
           return true;
         };
@@ -839,7 +970,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             }
           };
           if (ok && n_mine > 0) {
-            ok = ptx::mbar_wait(&bs->k_full[kvm % C::KST], (kvm / C::KST) & 1) && lock();
+            ok = ptx::mbar_wait(&kready[kvm % C::KST], (kvm / C::KST) & 1) && lock();
             if (ok) {
               ptx::tc_fence_after();
               issue_qk(kvm);
@@ -853,8 +984,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             const int vst = vr.stage(j);
             const bool more = j + 1 < n_mine;
             if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) ||
-                !ptx::mbar_wait(&bs->v_full[vst], vr.use(j) & 1) ||
-                (more && !ptx::mbar_wait(&bs->k_full[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) ||
+                !ptx::mbar_wait(&vready[vst], vr.use(j) & 1) ||
+                (more && !ptx::mbar_wait(&kready[(kv + 1) % C::KST], ((kv + 1) / C::KST) & 1)) ||
                 !lock()) {
               ok = false;
               break;
@@ -905,7 +1036,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           if (ok && n_mine > 0) {
             const uint32_t kv0 = kvm + ti;
             ok = (ti == 0 || ack_k1(0)) &&
-                 ptx::mbar_wait(&bs->k_full[kv0 % C::KST], (kv0 / C::KST) & 1) && lock();
+                 ptx::mbar_wait(&kready[kv0 % C::KST], (kv0 / C::KST) & 1) && lock();
             if (ok) {
               ptx::tc_fence_after();
               issue_qk(kv0);
@@ -922,9 +1053,9 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             // the other pipeline's V of block t - 1 and K of block t + 1 come
             // before this one's V of block t and K of block t + 2
             if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) || (t > 0 && !ack_v1(t - 1)) ||
-                !ptx::mbar_wait(&bs->v_full[vst], vr.use(t) & 1) ||
+                !ptx::mbar_wait(&vready[vst], vr.use(t) & 1) ||
                 (more && (!ack_k1(t + 1) ||
-                          !ptx::mbar_wait(&bs->k_full[(kv + 2) % C::KST], ((kv + 2) / C::KST) & 1))) ||
+                          !ptx::mbar_wait(&kready[(kv + 2) % C::KST], ((kv + 2) / C::KST) & 1))) ||
                 !lock()) {
               ok = false;
               break;
@@ -987,7 +1118,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     const uint32_t tS = tmem + ti * 128 + lane_off;
     const uint32_t tO = tmem + 256 + ti * 128 + lane_off;
     const float sl2 = p.scale_log2;
+    constexpr bool F16 = KVM != 0;
+    const bool of16 = out_f16<KVM>(p);
     uint32_t scnt = 0, ocnt = 0, wgp = 0, nfin = 0;
+    uint32_t kvs = 0;  // K/V tiles of the items before this one (all roles agree)
     VRing vr;
     bool ok = true;
     for (int n = 0; ok; ++n) {
@@ -1003,6 +1137,45 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
       const int n_mine = (ti ? it.n_mine[1] : it.n_mine[0]);
       const int ctx = it.ctx;
       vr.begin(it.kind);
+      // E4M3 cache: widen the item's fills, in the producer's order, up to
+      // fill `last` (this warp: page `warp` of each tile).  Every softmax warp
+      // takes part in every fill, so each observes every fill of every stage.
+      int cf = 0;
+      auto widen_through = [&](int last) -> bool {
+        const int nf = 2 * it.n_tiles;
+        for (; cf <= last && cf < nf; ++cf) {
+          bool is_v;
+          int t;
+          fill_of(cf, it.n_tiles, is_v, t);
+          unsigned char *stage;
+          uint64_t *full, *conv;
+          uint32_t par;
+          if (is_v) {
+            const int st = vr.stage(t);
+            stage = v_stage(st);
+            full = &bs->v_full[st];
+            conv = &bs->v_conv[st];
+            par = vr.use(t) & 1;
+          } else {
+            const uint32_t kc = kvs + t;
+            stage = sK + (kc % C::KST) * C::KV_BYTES;
+            full = &bs->k_full[kc % C::KST];
+            conv = &bs->k_conv[kc % C::KST];
+            par = (kc / C::KST) & 1;
+          }
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(full, par))) return false;
+          const int key0 = (it.page0 + 8 * (it.j0 + t) + warp) * kPage;  // this page's first key
+          if (is_v)
+            widen_page<D>(stage + warp * C::PAGE_BYTES + C::V8_OFF, stage + warp * C::PAGE_BYTES,
+                          kPage * 128, ctx - key0, lane);
+          else
+            widen_page<D>(stage + warp * kPage * 128 + C::K8_OFF, stage + warp * kPage * 128,
+                          BN * 128, ctx - key0, lane);
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(conv);
+        }
+        return true;
+      };
       if (it.kind == KIND_CHUNK) {
         const int q_len = it.q_len;
         const int tok = (2 * it.mp + ti) * TM + r / G;  // index within the chunk
@@ -1010,6 +1183,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         const int last = row_valid ? ctx - q_len + tok : 0;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_mine; ++j, ++scnt) {
+          // the fills the MMAs after P_j need (V_j, K_{j+1}), before waiting S_j
+          if (KVM == 2 && !widen_through(2 * j + 2)) { ok = false; break; }
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->s_full[ti], scnt & 1))) { ok = false; break; }
           ptx::tc_fence_after();
           const int key0 = (it.j0 + j) * BN;
@@ -1053,11 +1228,11 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             ptx::tmem_ld32(tS + (c + 1) * 32, sb);
             ptx::tmem_wait_ld_regs(sa);
             if (diag) mask_chunk(sa, nvis - c * 32);
-            exp_chunk_regs(sa, sc2, nm2, rs2, w16);
+            exp_chunk_regs<F16>(sa, sc2, nm2, rs2, w16);
             ptx::tmem_st16(tS + c * 16, w16);
             ptx::tmem_wait_ld_regs(sb);
             if (diag) mask_chunk(sb, nvis - (c + 1) * 32);
-            exp_chunk_regs(sb, sc2, nm2, rs2, w16);
+            exp_chunk_regs<F16>(sb, sc2, nm2, rs2, w16);
             ptx::tmem_st16(tS + (c + 1) * 16, w16);
           }
           {
@@ -1067,8 +1242,9 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             l_run += rs0 + rs1;
           }
           // Cache slots at or past ctx in the last page may hold anything (NaN
-          // included) and 0 * NaN is NaN inside PV: zero those V rows first.
-          if (key0 + BN > ctx) {
+          // included) and 0 * NaN is NaN inside PV: zero those V rows first
+          // (an E4M3 cache: already zeroed by the widening).
+          if (KVM != 2 && key0 + BN > ctx) {
             const int vst = vr.stage(j);
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[vst], vr.use(j) & 1))) {
               ok = false;
@@ -1088,17 +1264,21 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           ptx::tc_fence_before();
           ptx::mbar_arrive(&bs->p_full[ti]);
         }
+        // the rest of the item's fills (the other query tile may read them)
+        if (KVM == 2 && ok && !widen_through(2 * it.n_tiles - 1)) ok = false;
         vr.end(it.n_tiles);
-        if (!ok || n_mine == 0) continue;
+        kvs += it.n_tiles;
+        if (!ok) break;
+        if (n_mine == 0) continue;
         // epilogue: O / l, or this unit's partial and, from the last unit of
         // the pair to finish, the merge of all of them
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->o_final[ti], ocnt & 1))) { ok = false; break; }
         ++ocnt;
         ptx::tc_fence_after();
         const int64_t orow = ((int64_t)(it.qs + tok) * p.Hq + it.g * G + r % G) * D;
-        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + orow;
+        uint16_t *out = static_cast<uint16_t *>(p.out) + orow;
         if (it.nsplit == 1) {
-          const float inv = 1.f / l_run;
+          const float inv = (KVM == 2 ? p.v_scale : 1.f) / l_run;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
@@ -1110,8 +1290,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
                 uint32_t wds[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h)
-                  wds[h] = ptx::pack_bf16x2(__uint_as_float(o[q4 * 8 + h * 2]) * inv,
-                                            __uint_as_float(o[q4 * 8 + h * 2 + 1]) * inv);
+                  wds[h] = pack_out2(__uint_as_float(o[q4 * 8 + h * 2]) * inv,
+                                     __uint_as_float(o[q4 * 8 + h * 2 + 1]) * inv, of16);
                 *reinterpret_cast<uint4 *>(out + c * 32 + q4 * 8) =
                     make_uint4(wds[0], wds[1], wds[2], wds[3]);
               }
@@ -1165,7 +1345,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           const float2 ml = __ldcg(&w.chunk_ml[((int64_t)(it.first_slot + u) * 2 + ti) * 128 + r]);
           L = fmaf(ml.y, ml.x == -INFINITY ? 0.f : ptx::ex2(ml.x - M), L);
         }
-        const float inv = 1.f / L;
+        const float inv = (KVM == 2 ? p.v_scale : 1.f) / L;
         // 32 output dims at a time over every contributor
 #pragma unroll 1
         for (int cg = 0; cg < D / 32; ++cg) {
@@ -1193,7 +1373,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             uint32_t wds[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h)
-              wds[h] = ptx::pack_bf16x2(acc[8 * c + 2 * h] * inv, acc[8 * c + 2 * h + 1] * inv);
+              wds[h] = pack_out2(acc[8 * c + 2 * h] * inv, acc[8 * c + 2 * h + 1] * inv, of16);
             *reinterpret_cast<uint4 *>(out + cg * 32 + c * 8) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
           }
         }
@@ -1207,6 +1387,9 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         unsigned char *pt = smem + C::OFF_PT + ti * 4096;
         for (int j = 0; j < n_mine; ++j, ++scnt) {
           const int blk = ti + 2 * j;
+          // the fills the MMAs after P_blk need (up to K_{blk+2}), before
+          // waiting S_blk
+          if (KVM == 2 && !widen_through(2 * blk + 3)) { ok = false; break; }
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->s_full[ti], scnt & 1))) { ok = false; break; }
           ptx::tc_fence_after();
           uint32_t sr[G];
@@ -1249,11 +1432,12 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             // P^T, K-major: row q, key r; [panel r/64][16 rows][64 keys] swizzled
             const uint32_t off = (r >> 6) * (kDecN * 128) + q * 128 +
                                  ((((r & 63) >> 3) ^ (q & 7)) << 4) + (r & 7) * 2;
-            *reinterpret_cast<__nv_bfloat16 *>(pt + off) = __float2bfloat16_rn(pq);
+            *reinterpret_cast<uint16_t *>(pt + off) = cvt_out(pq, F16);
           }
           // cache slots past ctx in the sequence's last page: zero their V rows
+          // (an E4M3 cache: already zeroed by the widening)
           const int key0 = (it.page0 + 8 * blk) * kPage;
-          if (key0 + BN > ctx && key0 < it.n_pages * kPage) {
+          if (KVM != 2 && key0 + BN > ctx && key0 < it.n_pages * kPage) {
             const int vst = vr.stage(blk);
             if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->v_full[vst], vr.use(blk) & 1))) {
               ok = false;
@@ -1273,7 +1457,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           ptx::tc_fence_before();
           ptx::mbar_arrive(&bs->p_full[ti]);
         }
+        // the rest of the item's fills (the other pipeline's last blocks)
+        if (KVM == 2 && ok && !widen_through(2 * it.n_tiles - 1)) ok = false;
         vr.end(it.n_tiles);
+        kvs += it.n_tiles;
         if (!ok) break;
         if (n_mine > 0) {
           if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bs->o_final[ti], ocnt & 1))) { ok = false; break; }
@@ -1340,11 +1527,12 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           O[q] = __uint_as_float(o0[q]) * a0[q] + (other ? __uint_as_float(o1[q]) * a1[q] : 0.f);
         const int d = r;  // O^T lane = head dim
         const int64_t obase = ((int64_t)it.qs * p.Hq + it.g * G) * D;
-        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + obase;
+        uint16_t *out = static_cast<uint16_t *>(p.out) + obase;
         if (it.nsplit == 1) {
           if (d < D) {
 #pragma unroll
-            for (int q = 0; q < G; ++q) out[q * D + d] = __float2bfloat16_rn(O[q] / Lt[q]);
+            for (int q = 0; q < G; ++q)
+              out[q * D + d] = cvt_out(KVM == 2 ? O[q] * (p.v_scale / Lt[q]) : O[q] / Lt[q], of16);
           }
           continue;
         }
@@ -1383,7 +1571,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
         }
         if (d < D) {
 #pragma unroll
-          for (int q = 0; q < G; ++q) out[q * D + d] = __float2bfloat16_rn(acc[q] / Ls[q]);
+          for (int q = 0; q < G; ++q)
+            out[q * D + d] = cvt_out(KVM == 2 ? acc[q] * (p.v_scale / Ls[q]) : acc[q] / Ls[q], of16);
         }
       }
     }
@@ -1412,79 +1601,101 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int D, int G>
+template <int KVM, int D, int G>
 cudaError_t launch_dg(const AttnParams &p, const StepWs &w, cudaStream_t stream) {
   using C = StepCfg<D>;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap tq, tqd, tk, tv;
   // q viewed as [T][Hq][D]: chunk box = 64 dims x G heads x BM/G tokens,
-  // decode box = 64 dims x G heads x 1 token
+  // decode box = 64 dims x G heads x 1 token.  E4M3 cache: the binary16
+  // queries (the caller's, or the plan kernel's copy of bf16 ones).
   {
+    const void *qsrc = (KVM == 2 && !p.act_f16) ? p.q16 : p.q;
+    const CUtensorMapDataType qt =
+        KVM == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.num_tokens};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G)};
     cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.q), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (encode(&tq, qt, 3, const_cast<void *>(qsrc), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     box[2] = 1;
-    if (encode(&tqd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.q), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (encode(&tqd, qt, 3, const_cast<void *>(qsrc), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   const int64_t rows = p.num_pages * p.Hkv * kPage;
-  {
-    // K: cache rows [rows][D], box = one 64-dim panel of one page (16 rows)
+  if (KVM == 2) {
+    // E4M3 caches: rows of D one-byte codes, box = one page (16 rows),
+    // unswizzled (the widening reads it row-major)
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)D};
+    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kPage};
     cuuint32_t estr[2] = {1, 1};
-    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(p.k_cache), dims,
-               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(p.k_cache), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  }
-  {
-    // V: the same rows viewed as (64 dims, row, panel), box = a whole page with
-    // its panels outermost, [panel][16 rows][64 dims] in shared memory
-    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)C::PANELS};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
-    cuuint32_t box[3] = {64, (cuuint32_t)kPage, (cuuint32_t)C::PANELS};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.v_cache), dims,
-               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (encode(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(p.v_cache), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
+  } else {
+    const CUtensorMapDataType kt =
+        KVM == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    {
+      // K: cache rows [rows][D], box = one 64-dim panel of one page (16 rows)
+      cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+      cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+      cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+      cuuint32_t estr[2] = {1, 1};
+      if (encode(&tk, kt, 2, const_cast<void *>(p.k_cache), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    {
+      // V: the same rows viewed as (64 dims, row, panel), box = a whole page
+      // with its panels outermost, [panel][16 rows][64 dims] in shared memory
+      cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)C::PANELS};
+      cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+      cuuint32_t box[3] = {64, (cuuint32_t)kPage, (cuuint32_t)C::PANELS};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (encode(&tv, kt, 3, const_cast<void *>(p.v_cache), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
   }
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_step_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(attn_step_kernel<KVM, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  // the plan (and, fused, the append) ...
-  int append_ctas = 0;
-  if (p.fused) {
-    const int64_t pieces = (int64_t)p.num_tokens * p.Hkv * (D * 2 / 16);
-    append_ctas = (int)std::min<int64_t>(w.grid, (pieces + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
-  }
+  // the plan (with its side work: the fused append, the queries' copy) ...
+  const int64_t side = plan_append_pieces<KVM>(p) + plan_q_pieces<KVM>(p);
+  const int side_ctas = (int)std::min<int64_t>(w.grid, (side + 4 * kPlanThreads - 1) / (4 * kPlanThreads));
   static bool plan_configured = false;
   if (!plan_configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_plan_kernel<G>,
+    cudaError_t e = cudaFuncSetAttribute(attn_plan_kernel<KVM, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)plan_smem_bytes(kDecodeMaxSeqs));
     if (e != cudaSuccess) return e;
     plan_configured = true;
   }
-  attn_plan_kernel<G><<<1 + append_ctas, kPlanThreads, plan_smem_bytes(p.num_seqs), stream>>>(p, w);
+  attn_plan_kernel<KVM, G><<<1 + side_ctas, kPlanThreads, plan_smem_bytes(p.num_seqs), stream>>>(p, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // ... then the step, allowed to start while the plan finishes
@@ -1498,32 +1709,27 @@ cudaError_t launch_dg(const AttnParams &p, const StepWs &w, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_step_kernel<D, G>, p, w, tq, tqd, tk, tv, (int)rows);
+  return cudaLaunchKernelEx(&cfg, attn_step_kernel<KVM, D, G>, p, w, tq, tqd, tk, tv, (int)rows);
 }
 
 }  // namespace
 
-bool step_path(int dtype, int D, int G) {
-  if (dtype != CPA_BF16) return false;
-  if (D != 64 && D != 128) return false;
-  return G == 1 || G == 2 || G == 4 || G == 8;
-}
-
-cudaError_t launch_attention_step(const AttnParams &p, const StepWs &w, cudaStream_t stream) {
+template <int KVM>
+cudaError_t launch_step(const AttnParams &p, const StepWs &w, cudaStream_t stream) {
   const int G = p.Hq / p.Hkv;
   if (p.D == 128) {
     switch (G) {
-      case 1: return launch_dg<128, 1>(p, w, stream);
-      case 2: return launch_dg<128, 2>(p, w, stream);
-      case 4: return launch_dg<128, 4>(p, w, stream);
-      case 8: return launch_dg<128, 8>(p, w, stream);
+      case 1: return launch_dg<KVM, 128, 1>(p, w, stream);
+      case 2: return launch_dg<KVM, 128, 2>(p, w, stream);
+      case 4: return launch_dg<KVM, 128, 4>(p, w, stream);
+      case 8: return launch_dg<KVM, 128, 8>(p, w, stream);
     }
   } else {
     switch (G) {
-      case 1: return launch_dg<64, 1>(p, w, stream);
-      case 2: return launch_dg<64, 2>(p, w, stream);
-      case 4: return launch_dg<64, 4>(p, w, stream);
-      case 8: return launch_dg<64, 8>(p, w, stream);
+      case 1: return launch_dg<KVM, 64, 1>(p, w, stream);
+      case 2: return launch_dg<KVM, 64, 2>(p, w, stream);
+      case 4: return launch_dg<KVM, 64, 4>(p, w, stream);
+      case 8: return launch_dg<KVM, 64, 8>(p, w, stream);
     }
   }
   return cudaErrorInvalidValue;

@@ -8,6 +8,14 @@ namespace cpa {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The persistent step kernel takes every supported shape with 16-bit queries;
+// fp32 runs on the row kernel.
+bool step_path(int dtype, int D, int G) {
+  if (dtype != CPA_BF16 && dtype != CPA_F16) return false;
+  if (D != 64 && D != 128) return false;
+  return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
 int sm_count(int device) {
   static int sms[64] = {};
   if (device < 0 || device >= 64) return 0;
@@ -63,6 +71,10 @@ WorkspaceLayout workspace_layout(const cpa_desc &d, int num_seqs) {
   off = align_up(off + sizeof(float) * (size_t)w.cap_split * 2 * 128 * D, 256);
   w.chunk_ml = off;
   off = align_up(off + sizeof(float2) * (size_t)w.cap_split * 2 * 128, 256);
+  if (d.kv_dtype == CPA_KV_E4M3 && d.dtype == CPA_BF16) {
+    w.q16 = off;
+    off = align_up(off + 2 * (size_t)tok * d.num_q_heads * D, 256);
+  }
   w.total = off;
   w.clear = 256;  // the status word; the plan kernel zeroes the rest it uses
   return w;
@@ -75,7 +87,14 @@ static int check_shape(const cpa_desc *d) {
       d->page_size <= 0 || d->num_pages <= 0 || d->num_tokens < 0)
     return CPA_ERR_ARG;
   if (d->num_q_heads % d->num_kv_heads != 0) return CPA_ERR_ARG;
-  if (d->dtype != CPA_F32 && d->dtype != CPA_BF16) return CPA_ERR_UNSUPPORTED;
+  if (d->dtype != CPA_F32 && d->dtype != CPA_BF16 && d->dtype != CPA_F16)
+    return CPA_ERR_UNSUPPORTED;
+  if (d->kv_dtype != CPA_KV_SAME && d->kv_dtype != CPA_KV_E4M3) return CPA_ERR_UNSUPPORTED;
+  if (d->kv_dtype == CPA_KV_E4M3) {
+    if (d->dtype == CPA_F32) return CPA_ERR_UNSUPPORTED;  // 16-bit queries only
+    const float ks = d->k_scale, vs = d->v_scale;
+    if (!(ks > 0.f) || !(vs > 0.f) || ks > 3.0e38f || vs > 3.0e38f) return CPA_ERR_ARG;
+  }
   if (d->head_dim != 64 && d->head_dim != 128) return CPA_ERR_UNSUPPORTED;
   if (d->page_size != 16) return CPA_ERR_UNSUPPORTED;
   const int G = d->num_q_heads / d->num_kv_heads;
@@ -122,10 +141,12 @@ extern "C" int cpa_kv_append(const void *k, const void *v, const int64_t *slot_m
     if (!aligned(desc->workspace, 256) || desc->workspace_bytes < 256) return CPA_ERR_WORKSPACE;
     status = static_cast<uint32_t *>(desc->workspace);
   }
-  const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
+  const int eb = desc->dtype == CPA_F32 ? 4 : 2;
+  const int quant = desc->kv_dtype == CPA_KV_E4M3 ? (desc->dtype == CPA_F16 ? 2 : 1) : 0;
   cudaError_t e = launch_kv_append(k, v, slot_mapping, k_cache, v_cache, desc->num_tokens,
                                    desc->num_kv_heads, desc->head_dim, desc->page_size,
-                                   desc->num_pages, eb, status, (cudaStream_t)stream);
+                                   desc->num_pages, eb, quant, desc->k_scale, desc->v_scale,
+                                   status, (cudaStream_t)stream);
   return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }
 
@@ -175,7 +196,13 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
   p.page_size = desc->page_size;
   p.num_pages = desc->num_pages;
   p.max_pages = desc->max_pages_per_seq;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.act_f16 = desc->dtype == CPA_F16;
+  p.kv_e4m3 = desc->kv_dtype == CPA_KV_E4M3;
+  p.k_scale = p.kv_e4m3 ? desc->k_scale : 1.f;
+  p.v_scale = p.kv_e4m3 ? desc->v_scale : 1.f;
+  // scores live in the log2 domain; an E4M3 cache's K scale folds in here
+  p.scale_log2 = scale * p.k_scale * 1.4426950408889634f;
+  if (!(p.scale_log2 > 0.f) || p.scale_log2 > 3.0e38f) return CPA_ERR_ARG;
   p.max_splits = w.max_splits;
   p.status = reinterpret_cast<uint32_t *>(ws);
   cudaStream_t st = (cudaStream_t)stream;
@@ -213,14 +240,19 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
       p.v_new = nr.v;
       p.slot_mapping = nr.slots;
     }
-    return launch_attention_step(p, sw, st) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
+    if (w.q16) p.q16 = ws + w.q16;
+    cudaError_t e;
+    if (p.kv_e4m3) e = launch_step<2>(p, sw, st);
+    else if (p.act_f16) e = launch_step<1>(p, sw, st);
+    else e = launch_step<0>(p, sw, st);
+    return e == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
   }
   // row kernel: the append (if any) first, on the same stream
   if (nr.k) {
-    const int eb = desc->dtype == CPA_BF16 ? 2 : 4;
+    // fp32 only (every 16-bit shape runs on the step kernel): a plain copy
     if (launch_kv_append(nr.k, nr.v, nr.slots, const_cast<void *>(k_cache),
                          const_cast<void *>(v_cache), desc->num_tokens, p.Hkv, p.D,
-                         p.page_size, p.num_pages, eb, p.status, st) != cudaSuccess)
+                         p.page_size, p.num_pages, 4, 0, 1.f, 1.f, p.status, st) != cudaSuccess)
       return CPA_ERR_CUDA;
   }
   // the split-merge counters start at zero in every call, whatever an earlier

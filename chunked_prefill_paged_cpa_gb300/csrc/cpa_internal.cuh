@@ -24,13 +24,14 @@ enum : uint32_t {
 //      counters  uint32 [num_seqs * Hkv]      split-merge arrival counts
 //      part_o / part_ml  one partial (o, (max, sum)) per (sequence, query
 //                        head, split of kSplitKeys keys)
-//  - Step kernel (bf16, head_dim 64/128, GQA group 1/2/4/8):
+//  - Step kernel (16-bit queries, head_dim 64/128, GQA group 1/2/4/8):
 //      header    status word; queue sizes, decode slice pages, ticket
 //      list      the step's work queue, one 32-byte entry per item
 //      dec_ctr   uint32 [num_seqs * Hkv]      decode segments' arrival counts
 //      chunk_ctr uint32 [2 * chunk units]     per (tile pair, tile) counts
 //      dec_o / dec_ml   one partial per decode slice: G rows x D, (max, sum)
 //      chunk_o / chunk_ml  one partial per split chunk unit: two 128-row tiles
+//      q16       E4M3 cache with bf16 queries: their binary16 copy [T][Hq][D]
 //    Capacities, for a grid of up to kMaxStepGrid CTAs: decode slices <=
 //    Hkv * num_seqs + 32 * kMaxStepGrid; chunk units <= max(kMaxStepGrid,
 //    Hkv * (ceil(num_tokens * G / 256) + num_seqs)); split chunk units <=
@@ -44,7 +45,7 @@ struct WorkspaceLayout {
   size_t counters, part_o, part_ml;
   int max_splits;
   // step kernel
-  size_t list, dec_ctr, chunk_ctr, dec_o, dec_ml, chunk_o, chunk_ml;
+  size_t list, dec_ctr, chunk_ctr, dec_o, dec_ml, chunk_o, chunk_ml, q16;
   int cap_dec, cap_chunk, cap_split;
 };
 
@@ -96,6 +97,13 @@ struct AttnParams {
   const void *k_new;
   const void *v_new;
   const int64_t *slot_mapping;
+  // Element types: act_f16 = q, k/v rows and out are binary16 (else bf16 on
+  // the step kernel); kv_e4m3 = the caches hold E4M3 codes of K / k_scale and
+  // V / v_scale; q16 = the plan kernel's binary16 copy of bf16 queries.
+  int act_f16;
+  int kv_e4m3;
+  float k_scale, v_scale;
+  void *q16;
   uint32_t *status;
   uint32_t *counters;
   float *part_o;
@@ -116,19 +124,25 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
               const int32_t *seq_lens, int32_t num_seqs, float scale, void *out,
               void *stream, const cpa_desc *desc, const NewRows &nr, size_t clear_bytes);
 
+// Append of new rows; `quant` 0: copy elem_bytes-wide elements; 1 / 2: E4M3
+// codes of bf16 / binary16 rows divided by k_scale (K) and v_scale (V).
 cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
                              void *k_cache, void *v_cache, int64_t num_tokens,
                              int Hkv, int D, int page_size, int64_t num_pages,
-                             int elem_bytes, uint32_t *status, cudaStream_t stream);
+                             int elem_bytes, int quant, float k_scale, float v_scale,
+                             uint32_t *status, cudaStream_t stream);
 
 cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t stream);
 
 // Number of SMs of a device (cached); 0 if it cannot be queried.
 int sm_count(int device);
 
-// The step kernel (attn_step.cu): bf16, head_dim 64/128, GQA group 1/2/4/8.
+// The step kernel (attn_step.cuh, one translation unit per cache mode):
+// 16-bit queries, head_dim 64/128, GQA group 1/2/4/8.  KVM 0: bf16 queries and
+// caches; 1: binary16 queries and caches; 2: E4M3 caches.
 bool step_path(int dtype, int D, int G);
-cudaError_t launch_attention_step(const AttnParams &p, const StepWs &w, cudaStream_t stream);
+template <int KVM>
+cudaError_t launch_step(const AttnParams &p, const StepWs &w, cudaStream_t stream);
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -2,6 +2,8 @@
 // proxy fences, packed fp32 math.  Every wait is bounded.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <stdint.h>
 
 namespace cpa {
@@ -333,10 +335,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void *smem, uint32_t l
 
 // Instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
+                                                      bool b_mn_major, bool f16 = false) {
   return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+         | ((f16 ? 0u : 1u) << 7)        // A format: bf16 (1) or f16 (0)
+         | ((f16 ? 0u : 1u) << 10)       // B format: bf16 (1) or f16 (0)
          | ((a_mn_major ? 1u : 0u) << 15)
          | ((b_mn_major ? 1u : 0u) << 16)
          | ((uint32_t)(N >> 3) << 17)
@@ -387,6 +389,55 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---- OCP FP8 E4M3 ------------------------------------------------------------
+
+// Four E4M3 codes (low byte first) to four binary16 values, two per word (the
+// lower code in the lower half).  Exact: every E4M3 value is a binary16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+}
+// Two fp32 values to two E4M3 codes (lo in the low byte): nearest, ties to
+// even, out-of-range values and infinities saturated to +-448, NaN to NaN.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight 16-bit values (bf16, or binary16 when F16), each divided by `scale`
+// (one correctly rounded binary32 division), as eight E4M3 codes.
+template <bool F16>
+__device__ __forceinline__ uint2 quantise8_e4m3(uint4 x, float scale) {
+  const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t b[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t w = in[2 * h + q];
+      float lo, hi;
+      if (F16) {
+        lo = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+        hi = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+      } else {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+      }
+      b[q] = f32x2_to_e4m3x2(__fdiv_rn(lo, scale), __fdiv_rn(hi, scale));
+    }
+    out[h] = b[0] | (b[1] << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
 // Two bf16 (packed in a 32-bit word, low element first) widened to an fp32 pair.
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));

@@ -18,7 +18,8 @@ from . import build as _build
 
 CPA_OK, CPA_ERR_ARG, CPA_ERR_UNSUPPORTED, CPA_ERR_WORKSPACE, CPA_ERR_CUDA, CPA_ERR_DEVICE = (
     0, -1, -2, -3, -4, -5)
-CPA_F32, CPA_BF16 = 0, 1
+CPA_F32, CPA_BF16, CPA_F16 = 0, 1, 2
+CPA_KV_SAME, CPA_KV_E4M3 = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -36,6 +37,9 @@ class CpaDesc(ctypes.Structure):
         ("num_tokens", ctypes.c_int64),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -161,6 +165,8 @@ def _dtype_code(dtype: torch.dtype) -> int:
         return CPA_BF16
     if dtype == torch.float32:
         return CPA_F32
+    if dtype == torch.float16:
+        return CPA_F16
     raise TypeError(f"unsupported dtype {dtype}")
 
 
@@ -175,28 +181,39 @@ def _stream(stream):
 
 
 def make_desc(k_cache: torch.Tensor, num_q_heads: int, num_tokens: int,
-              max_pages_per_seq: int, workspace: torch.Tensor | None = None) -> CpaDesc:
+              max_pages_per_seq: int, workspace: torch.Tensor | None = None,
+              act_dtype: torch.dtype | None = None, k_scale: float = 1.0,
+              v_scale: float = 1.0) -> CpaDesc:
+    """Descriptor for a cache tensor: a uint8 cache holds E4M3 codes (its
+    activations then have ``act_dtype``, bf16 by default, and the codes the
+    per-tensor scales); any other cache holds the activation dtype."""
     num_pages, Hkv, page, D = k_cache.shape
+    e4m3 = k_cache.dtype == torch.uint8
+    dt = (act_dtype or torch.bfloat16) if e4m3 else k_cache.dtype
     return CpaDesc(int(num_q_heads), int(Hkv), int(D), int(page), int(num_pages),
-                   int(max_pages_per_seq), _dtype_code(k_cache.dtype), int(num_tokens),
+                   int(max_pages_per_seq), _dtype_code(dt), int(num_tokens),
                    None if workspace is None else workspace.data_ptr(),
-                   0 if workspace is None else workspace.numel() * workspace.element_size())
+                   0 if workspace is None else workspace.numel() * workspace.element_size(),
+                   CPA_KV_E4M3 if e4m3 else CPA_KV_SAME,
+                   float(k_scale) if e4m3 else 0.0, float(v_scale) if e4m3 else 0.0)
 
 
 def workspace_for(k_cache: torch.Tensor, num_q_heads: int, max_pages_per_seq: int,
-                  num_seqs: int, num_tokens: int) -> torch.Tensor:
+                  num_seqs: int, num_tokens: int,
+                  act_dtype: torch.dtype | None = None) -> torch.Tensor:
     """A zero-filled device workspace sized by cpa_workspace_bytes for steps of
     at most ``num_seqs`` sequences and ``num_tokens`` packed tokens on the
-    current device."""
-    desc = make_desc(k_cache, num_q_heads, num_tokens, max_pages_per_seq)
+    current device (``act_dtype``: the queries' dtype for a uint8 E4M3 cache)."""
+    desc = make_desc(k_cache, num_q_heads, num_tokens, max_pages_per_seq, act_dtype=act_dtype)
     n = cpa_workspace_bytes(desc, num_seqs)
     if n == 0:
         raise CpaError(CPA_ERR_ARG, "cpa_workspace_bytes")
     return torch.zeros(n, dtype=torch.uint8, device=k_cache.device)
 
 
-def kv_append(k, v, slot_mapping, k_cache, v_cache, workspace=None, stream=None) -> None:
-    desc = make_desc(k_cache, 1, k.shape[0], 1, workspace)
+def kv_append(k, v, slot_mapping, k_cache, v_cache, workspace=None, stream=None,
+              k_scale=1.0, v_scale=1.0) -> None:
+    desc = make_desc(k_cache, 1, k.shape[0], 1, workspace, k.dtype, k_scale, v_scale)
     desc.num_q_heads = desc.num_kv_heads
     rc = cpa_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                        desc, _stream(stream))
@@ -205,10 +222,11 @@ def kv_append(k, v, slot_mapping, k_cache, v_cache, workspace=None, stream=None)
 
 
 def attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq_lens, scale,
-                      workspace, out=None, stream=None) -> torch.Tensor:
+                      workspace, out=None, stream=None, k_scale=1.0, v_scale=1.0) -> torch.Tensor:
     if out is None:
         out = torch.empty_like(q)
-    desc = make_desc(k_cache, q.shape[1], q.shape[0], block_table.shape[1], workspace)
+    desc = make_desc(k_cache, q.shape[1], q.shape[0], block_table.shape[1], workspace,
+                     q.dtype, k_scale, v_scale)
     rc = cpa_attention_forward(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                _ptr(query_start_loc), _ptr(seq_lens), seq_lens.shape[0],
                                scale, _ptr(out), _stream(stream), desc)
@@ -219,12 +237,13 @@ def attention_forward(q, k_cache, v_cache, block_table, query_start_loc, seq_len
 
 def append_attention_forward(q, k, v, slot_mapping, k_cache, v_cache, block_table,
                              query_start_loc, seq_lens, scale, workspace, out=None,
-                             stream=None) -> torch.Tensor:
+                             stream=None, k_scale=1.0, v_scale=1.0) -> torch.Tensor:
     """kv_append followed by attention_forward, as one C-ABI call (the append
     fused into the attention kernels where they take the shape)."""
     if out is None:
         out = torch.empty_like(q)
-    desc = make_desc(k_cache, q.shape[1], q.shape[0], block_table.shape[1], workspace)
+    desc = make_desc(k_cache, q.shape[1], q.shape[0], block_table.shape[1], workspace,
+                     q.dtype, k_scale, v_scale)
     rc = cpa_append_attention_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(slot_mapping),
                                       _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                       _ptr(query_start_loc), _ptr(seq_lens), seq_lens.shape[0],

@@ -147,15 +147,31 @@ def free_ride(chunk: int, seed: int = 0) -> Scenario:
 NAMES = ["tiny", "page1_default", "large_budget", "long_context", "decode_only"]
 
 
+# Per-tensor scales of the 8-bit (E4M3) cache variant of the workloads: K/V
+# entries are N(0, 1), so |x| / 2^-6 stays below the format's 448 up to
+# |x| = 7 while values down to 2^-12 keep E4M3's full 3-bit mantissa.
+E4M3_SCALES = (2.0 ** -6, 2.0 ** -6)
+
+
+def e4m3_codes(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """OCP FP8 E4M3 codes (uint8) of x / scale (state preparation for the
+    prefix a step finds in an 8-bit cache): torch's float32 division and
+    round-to-nearest-even cast, with saturation at +-448."""
+    y = (x.float() / torch.tensor(scale, dtype=torch.float32, device=x.device)).clamp(-448.0, 448.0)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 class WorkloadState:
     """Device-resident state of a scenario: per-position Q/K/V, the page pool
     (physical pages in random order, 1.25x the need, unused pages poisoned with
     NaN), and the paged caches holding every sequence's prefix as the first
     step finds it.  Steps are then fed in order; the caller appends each step's
-    new K/V (``cpa_kv_append``) before attending."""
+    new K/V (``cpa_kv_append``) before attending.  With ``kv_e4m3`` = (k_scale,
+    v_scale) the caches are uint8 E4M3 codes (unused pages poisoned with the
+    NaN code)."""
 
     def __init__(self, sc: Scenario, device="cpu", pool_factor: float = 1.25,
-                 tensor_device=None):
+                 tensor_device=None, kv_e4m3=None):
         self.sc = sc
         sh = sc.shape
         self.device = torch.device(device)
@@ -173,10 +189,15 @@ class WorkloadState:
         self.paged = PagedSeqs(self.alloc, sh.page_size)
         self.num_pages = pool
         cache_shape = (pool, sh.num_kv_heads, sh.page_size, sh.head_dim)
-        self.k_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
-                                  device=self.device)
-        self.v_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
-                                  device=self.device)
+        self.kv_e4m3 = kv_e4m3
+        if kv_e4m3:
+            self.k_cache = torch.full(cache_shape, 0x7f, dtype=torch.uint8, device=self.device)
+            self.v_cache = torch.full(cache_shape, 0x7f, dtype=torch.uint8, device=self.device)
+        else:
+            self.k_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
+                                      device=self.device)
+            self.v_cache = torch.full(cache_shape, float("nan"), dtype=sh.dtype,
+                                      device=self.device)
         # prefix each sequence already has in the cache when it first appears
         for plan in sc.plans:
             for s in plan.seqs:
@@ -187,6 +208,8 @@ class WorkloadState:
                 if pre > 0:
                     pos = torch.arange(pre)
                     k, v = self.kv_rows(s.rid, pos)
+                    if kv_e4m3:
+                        k, v = e4m3_codes(k, kv_e4m3[0]), e4m3_codes(v, kv_e4m3[1])
                     write_positions(self.k_cache, self.v_cache, pl, pos, k, v)
 
     def kv_rows(self, rid, positions: torch.Tensor):

@@ -29,7 +29,9 @@
  *      query_start_loc   int32 [num_seqs + 1], query_start_loc[0] == 0
  *      seq_lens          int32 [num_seqs]
  *      slot_mapping      int64 [num_tokens]
- *    Element type of q, k, v, caches and out: `dtype` (fp32 or bf16).
+ *    Element type of q, k, v and out: `dtype` (fp32, bf16 or fp16).  The
+ *    caches hold `dtype` too, or, with desc->kv_dtype = CPA_KV_E4M3 (16-bit
+ *    dtypes only), one OCP FP8 E4M3 code per element (see cpa_kv_dtype).
  *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
  *  - Supported: head_dim 64 or 128, page_size 16, num_q_heads a multiple of
  *    num_kv_heads with a group of 1, 2, 4 or 8 heads.
@@ -69,7 +71,27 @@ typedef enum {
  * completion in time (for instance a stream starved for longer than the wait
  * limit by other work); the same call can simply be issued again. */
 
-typedef enum { CPA_F32 = 0, CPA_BF16 = 1 } cpa_dtype;
+typedef enum { CPA_F32 = 0, CPA_BF16 = 1, CPA_F16 = 2 } cpa_dtype;
+
+/* Storage of the paged caches.
+ *  CPA_KV_SAME  the caches hold `dtype` elements, bit for bit what was
+ *               appended.
+ *  CPA_KV_E4M3  the caches hold one byte per element: the OCP 8-bit floating
+ *               point (OFP8) E4M3 code of the value divided by a per-tensor
+ *               scale (desc->k_scale for K, desc->v_scale for V); the cached
+ *               K is k_scale * E4M3 value, V likewise.  The append computes
+ *               x / scale as one correctly rounded binary32 division, then
+ *               rounds to the nearest E4M3 value (ties to even), saturating
+ *               at +-448 (infinities included); NaN gives a NaN code.  The
+ *               attention reads the codes exactly: the tensor cores multiply
+ *               their exact binary16 values, q rounded to binary16 (exact for
+ *               bf16 or fp16 inputs of magnitude 2^-17 .. 65504; larger
+ *               magnitudes overflow), the softmax weights in binary16, with
+ *               fp32 accumulation; k_scale is folded into the softmax scale
+ *               and v_scale into the output.  Halves the cache bytes a step
+ *               reads.  The pages do not cover an 8-bit cache: a library
+ *               extension. */
+typedef enum { CPA_KV_SAME = 0, CPA_KV_E4M3 = 1 } cpa_kv_dtype;
 
 /* Problem description shared by the calls.  Sizes are host values. */
 typedef struct cpa_desc {
@@ -89,6 +111,9 @@ typedef struct cpa_desc {
                                  state it uses (work queue, merge counters),
                                  whatever an earlier call left there          */
   size_t workspace_bytes;
+  int32_t kv_dtype;           /* cpa_kv_dtype; 0 = caches of `dtype`          */
+  float k_scale, v_scale;     /* CPA_KV_E4M3: positive finite per-tensor
+                                 scales; ignored otherwise                    */
 } cpa_desc;
 
 /* Human-readable name of a cpa_status value (static string, never NULL). */
@@ -107,13 +132,14 @@ size_t cpa_workspace_bytes(const cpa_desc *desc, int32_t num_seqs);
 /* KV append: for every packed token t with slot = slot_mapping[t] >= 0, copy
  * k[t][g][:] to k_cache[slot / page_size][g][slot % page_size][:] and likewise
  * v, for all kv heads g.  A negative slot skips the token.  The copy is
- * bit-exact.  ("Chunked Prefill on an M5 Max", section "Wiring it into the
+ * bit-exact (an E4M3 cache stores the codes of k / k_scale and v / v_scale,
+ * see cpa_kv_dtype).  ("Chunked Prefill on an M5 Max", section "Wiring it into the
  * loop": a chunk extends the cache instead of rebuilding it; "Chunked Prefill
  * 技术深度解析", section 4.2: 16-token pages.)
  * Slots >= num_pages * page_size are skipped and raise the device status word
  * when a workspace is given in desc.  Tokens must map to distinct slots.
- * Only desc->num_kv_heads, head_dim, page_size, num_pages, dtype, num_tokens
- * and (optionally) workspace are read. */
+ * Only desc->num_kv_heads, head_dim, page_size, num_pages, dtype, num_tokens,
+ * kv_dtype (with k_scale, v_scale) and (optionally) workspace are read. */
 int cpa_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
                   void *k_cache, void *v_cache, const cpa_desc *desc,
                   void *stream);

@@ -145,3 +145,27 @@ def test_noalloc_rejects_bad_arguments_before_touching_the_device(lib):
 
 def load_status_null(lib):
     return lib.cpa_noalloc_read_device_status(None, None)
+
+
+def test_cache_dtype_descriptions(lib):
+    # binary16 activations take the same shapes as bf16
+    assert ops.cpa_workspace_bytes(_desc(dtype=ops.CPA_F16), 8) == \
+        ops.cpa_workspace_bytes(_desc(), 8)
+    # an E4M3 cache: 16-bit activations only, positive finite scales
+    e = dict(kv_dtype=ops.CPA_KV_E4M3, k_scale=0.5, v_scale=2.0)
+    assert ops.cpa_workspace_bytes(_desc(**e, dtype=ops.CPA_F32), 8) == 0
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert ops.cpa_workspace_bytes(_desc(**dict(e, k_scale=ks, v_scale=vs)), 8) == 0
+    assert ops.cpa_workspace_bytes(_desc(kv_dtype=5), 8) == 0
+    # bf16 queries read by binary16 MMAs: room for their binary16 copy
+    T, Hq, D = 10, 32, 128
+    n_bf16 = ops.cpa_workspace_bytes(_desc(**e), 8)
+    n_f16 = ops.cpa_workspace_bytes(_desc(**e, dtype=ops.CPA_F16), 8)
+    assert n_f16 == ops.cpa_workspace_bytes(_desc(), 8)
+    assert n_bf16 == n_f16 + -(-2 * T * Hq * D // 256) * 256
+
+
+def test_e4m3_append_rejects_bad_scales_before_launch(lib):
+    d = _desc(kv_dtype=ops.CPA_KV_E4M3, k_scale=-1.0, v_scale=1.0)
+    buf = ctypes.c_void_p(0x1000)
+    assert ops.cpa_kv_append(buf, buf, ctypes.c_void_p(0x2000), buf, buf, d, None) == ops.CPA_ERR_ARG
