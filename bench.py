@@ -52,17 +52,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def step_counts(q_lens, seq_lens, Hq, Hkv, D, elem_bytes):
+def step_counts(q_lens, seq_lens, Hq, Hkv, D, elem_bytes, kv_elem_bytes=None):
     """Algorithmic work of one attention step: FLOPs over causally visible
     (query, key) pairs (QK^T and PV, 2 FLOPs per multiply-add each) and bytes
-    (every sequence's K/V read once, Q read and O written once)."""
+    (every sequence's K/V read once, Q read and O written once).  An 8-bit
+    cache has kv_elem_bytes = 1."""
+    kb = elem_bytes if kv_elem_bytes is None else kv_elem_bytes
     pairs = 0
     for ql, sl in zip(q_lens, seq_lens):
         pairs += ql * (sl - ql) + ql * (ql + 1) // 2
     flops = 4 * D * Hq * pairs
-    kv_bytes = sum(seq_lens) * Hkv * D * elem_bytes * 2
+    kv_bytes = sum(seq_lens) * Hkv * D * kb * 2
     qo_bytes = sum(q_lens) * Hq * D * elem_bytes * 2
-    append_bytes = sum(q_lens) * Hkv * D * elem_bytes * 2 * 2   # read + write, K and V
+    append_bytes = sum(q_lens) * Hkv * D * (elem_bytes + kb) * 2   # read + write, K and V
     return {"pairs": pairs, "flops": flops, "bytes": kv_bytes + qo_bytes,
             "kv_bytes": kv_bytes, "append_bytes": append_bytes}
 
@@ -467,7 +469,8 @@ def run_gpu(args, world, rank, local):
         torch.cuda.empty_cache()
         line["workloads"] = measure_workloads(
             ["page1_default", "large_budget", "long_context", "decode_only", "oneshot_8192",
-             "tiny"], dev, flush, stream, peaks, args.steps, args.warmup, args.seed)
+             "tiny", "page1_default_e4m3", "long_context_e4m3", "decode_only_e4m3"],
+            dev, flush, stream, peaks, args.steps, args.warmup, args.seed)
         line["sweep"] = measure_sweep(dev, flush, stream, peaks, args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -493,19 +496,23 @@ def _fused_call(ws, inp, stream):
     from chunked_prefill_paged_cpa_gb300 import ops
     sh = ws.sc.shape
     m = inp["meta"]
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs,
+                            m.num_tokens, sh.dtype)
     out = torch.empty_like(inp["q"])
+    ks, vs = ws.kv_e4m3 or (1.0, 1.0)
 
     def call():
         ops.append_attention_forward(inp["q"], inp["k"], inp["v"], m.slot_mapping, ws.k_cache,
                                      ws.v_cache, m.block_table, m.query_start_loc, m.seq_lens,
-                                     sh.scale, wsp, out=out, stream=stream)
+                                     sh.scale, wsp, out=out, stream=stream, k_scale=ks,
+                                     v_scale=vs)
     return call
 
 
-def _roofline_entry(m, sh, us, peaks):
+def _roofline_entry(m, sh, us, peaks, kv_elem_bytes=None):
     eb = torch.empty((), dtype=sh.dtype).element_size()
-    c = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, eb)
+    c = step_counts(m.q_lens, m.seq_lens_list, sh.num_q_heads, sh.num_kv_heads, sh.head_dim, eb,
+                    kv_elem_bytes)
     t_b = c["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_f = c["flops"] / (peaks["bf16_tflops"] * 1e12)
     return c, {"roofline_us": max(t_b, t_f) * 1e6, "frac": max(t_b, t_f) * 1e6 / us,
@@ -517,12 +524,16 @@ def measure_workloads(names, dev, flush, stream, peaks, steps, warmup, seed):
     """Every named workload's first step through the fused call, timed like the
     headline (L2 flushed before each call, CUDA events on the launching
     stream): step time, query tokens/s and the fraction of the step roofline;
-    decode-only steps also report achieved HBM bandwidth."""
+    decode-only steps also report achieved HBM bandwidth.  A name ending in
+    _e4m3 is that workload over an 8-bit cache (OCP FP8 E4M3 codes, per-tensor
+    scales; bf16 queries), its bytes counted at one byte per cached element."""
     from chunked_prefill_paged_cpa_gb300 import workloads
     res = {}
     for name in names:
-        sc = workloads.scenario(name, seed)
-        ws = workloads.WorkloadState(sc, device=dev)
+        e4m3 = name.endswith("_e4m3")
+        sc = workloads.scenario(name[:-5] if e4m3 else name, seed)
+        ws = workloads.WorkloadState(sc, device=dev,
+                                     kv_e4m3=workloads.E4M3_SCALES if e4m3 else None)
         inp = ws.step(0)
         m = inp["meta"]
         sh = sc.shape
@@ -532,11 +543,14 @@ def measure_workloads(names, dev, flush, stream, peaks, steps, warmup, seed):
             call()
         us = _time_calls(call, flush, stream, steps)
         mean = sum(us) / len(us)
-        c, roof = _roofline_entry(m, sh, mean, peaks)
+        c, roof = _roofline_entry(m, sh, mean, peaks, 1 if e4m3 else None)
         e = {"step_us": mean, "step_us_min": min(us), "tokens_per_s": m.num_tokens / (mean * 1e-6),
              "query_tokens": m.num_tokens, "num_seqs": m.num_seqs,
              "kv_tokens": int(sum(m.seq_lens_list)),
              "dtype": "bf16" if sh.dtype == torch.bfloat16 else "f32"}
+        if e4m3:
+            e["kv_cache"] = {"format": "OCP FP8 E4M3", "k_scale": ws.kv_e4m3[0],
+                             "v_scale": ws.kv_e4m3[1]}
         if sh.dtype == torch.bfloat16:
             e["step_roofline"] = roof
         else:
