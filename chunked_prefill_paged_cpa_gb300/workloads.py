@@ -115,6 +115,11 @@ def scenario(name: str, seed: int = 0) -> Scenario:
     if name == "decode_only":
         L = synth.uniform_lengths(256, 2048, 8192, s_len)
         return _run(name, LLAMA3_8B, _decoders(L), [], 256, 1, seed, {"budget": 256})
+    if name == "decode_only_64":
+        # a quarter of decode_only (same length law, ~1.7 GB of cache): the
+        # size DRAM-counter captures run on, scaled to the full step
+        L = synth.uniform_lengths(64, 2048, 8192, s_len)
+        return _run(name, LLAMA3_8B, _decoders(L), [], 64, 1, seed, {"budget": 64})
     raise KeyError(name)
 
 

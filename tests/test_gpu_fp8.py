@@ -219,3 +219,43 @@ def test_full_size_e4m3(cuda_device, name, every):
     sd = m.slot_mapping
     want_k = oracle.e4m3_encode(inp["k"].cpu(), ks)
     assert torch.equal(ws.k_cache[sd // 16, :, sd % 16, :].cpu(), want_k)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "f16", "e4m3_bf16", "e4m3_f16"])
+def test_long_decode_slices_every_cache_mode(cuda_device, mode):
+    """Decode slices long enough for every pipeline to run its look-ahead
+    (several 128-key blocks per slice, slice lengths of every residue mod 4,
+    so the last fills of a slice meet the widening window in every position)
+    beside a chunk, in every cache mode."""
+    act = torch.float16 if mode.endswith("f16") else torch.bfloat16
+    e4m3 = mode.startswith("e4m3")
+    n = 12
+    q_lens = [1] * n + [48]
+    seq_lens = [6000 + 130 * i for i in range(n)] + [48 + 700]
+    ks, vs = 0.021, 0.043
+    D, Hq, Hkv = 128, 32, 8
+    scale = 1 / math.sqrt(D)
+    dev = cuda_device
+    if e4m3:
+        st = fp8_step(q_lens, seq_lens, Hq, Hkv, D, act, 5400, ks, vs)
+        kc, vc = st["kc8"].to(dev), st["vc8"].to(dev)
+    else:
+        st = make_step(q_lens, seq_lens, Hq, Hkv, D, act, 5400)
+        kc, vc = st["oracle_cache"].k.to(dev), st["oracle_cache"].v.to(dev)
+    m = st["meta"].to(dev)
+    q, k, v = st["q"].to(dev), st["k_new"].to(dev), st["v_new"].to(dev)
+    wsp = ops.workspace_for(kc, Hq, m.block_table.shape[1], m.num_seqs, m.num_tokens, act)
+    kw = dict(k_scale=ks, v_scale=vs) if e4m3 else {}
+    out = ops.append_attention_forward(q, k, v, m.slot_mapping, kc, vc, m.block_table,
+                                       m.query_start_loc, m.seq_lens, scale, wsp, **kw)
+    torch.cuda.synchronize()
+    assert ops.device_status(kc, Hq, m.block_table.shape[1], wsp) == 0
+    if e4m3:
+        want = oracle_fp8(st, ks, vs, scale)
+    else:
+        mc = st["meta"]
+        slots = oracle.slot_mapping(mc.block_table, mc.query_start_loc, mc.seq_lens, 16)
+        oracle.kv_append(st["oracle_cache"].k, st["oracle_cache"].v, st["k_new"], st["v_new"], slots)
+        want = oracle.attention(st["q"], st["oracle_cache"].k, st["oracle_cache"].v,
+                                mc.block_table, mc.query_start_loc, mc.seq_lens, scale)
+    assert_close(out.cpu(), want, f"long decode slices, {mode}")

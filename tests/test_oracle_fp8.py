@@ -190,7 +190,7 @@ FP8_MUTANTS = {
     "scale multiplied, not divided": ("float y = xi / scale;", "float y = xi * scale;"),
     "quotient by a reciprocal": ("float y = xi / scale;", "float y = xi * (1.0f / scale);"),
     "k_scale not applied": ("dot *= P->k_scale;", ""),
-    "v_scale not applied": ("out[d] += p * (P->v_scale * load_elem", "out[d] += p * (1.0 * load_elem"),
+    "v_scale not applied": ("double pv = p * P->v_scale;", "double pv = p;"),
     "append swaps the scales": ("D, k_scale, k_cache + dst);", "D, v_scale, k_cache + dst);"),
     "binary16 bias off by one": ("ldexp((double)(1024 + fr), ef - 25)", "ldexp((double)(1024 + fr), ef - 24)"),
 }
