@@ -77,13 +77,14 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;  // MMA issuers: warps 9 and 10
 constexpr int kItemSlots = 4;
 constexpr int kDecN = 16;        // N of the decode MMAs: the G query rows, padded
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;  // block size of the plan kernel (its side work)
+constexpr int kPlanWorkers = 256;   // threads of block 0 that build the queue
 // A tile pair's KV range is split over several units only into pieces of at
 // least this many KV tiles: each unit pays a query load, a pipeline fill and
 // a partial-result merge.
 constexpr int kMinUnitTiles = 8;
 // Decode slices are queued longest first, bucketed by their 8-page blocks.
-constexpr int kSizeBuckets = 1024;
+constexpr int kSizeBuckets = kPlanWorkers;
 
 enum : int { KIND_CHUNK = 0, KIND_DECODE = 1, KIND_DONE = 2 };
 
@@ -260,6 +261,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   // into shared memory; totals and per-sequence counts come from block scans;
   // the decode slices are ordered longest first by a count per size bucket
   // (one atomic per sequence); the entries are then written in parallel.
+  // Only the first kPlanWorkers threads: a smaller barrier settles faster
+  // (the queue is on the step's critical path); they sync on barrier 1.
+  if (tid >= kPlanWorkers) return;
+  auto sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kPlanWorkers) : "memory"); };
   extern __shared__ int plan_smem[];
   const int S = p.num_seqs, lane = tid & 31, warp = tid >> 5;
   const int Hkv = p.Hkv;
@@ -267,14 +272,14 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   int *s_dec = sq_ctx + S;     // [S + 1] exclusive bases of each sequence's slices
   int *s_chk = s_dec + S + 1;  // [S + 1] ... and of its chunk units
   int *s_pos = s_chk + S + 1;  // [S] first place of a decode sequence's slices, by size
-  __shared__ long long s_red[kPlanThreads / 32][3];
-  __shared__ int s_wd[kPlanThreads / 32], s_wc[kPlanThreads / 32];
+  __shared__ long long s_red[kPlanWorkers / 32][3];
+  __shared__ int s_wd[kPlanWorkers / 32], s_wc[kPlanWorkers / 32];
   __shared__ int s_hist[kSizeBuckets];
-  for (int b = tid; b < kSizeBuckets; b += kPlanThreads) s_hist[b] = 0;
+  for (int b = tid; b < kSizeBuckets; b += kPlanWorkers) s_hist[b] = 0;
 
   // pass 1: metadata, decode pages, chunk tile pairs and their KV tiles
   long long pages = 0, pairs = 0, ctiles = 0;
-  for (int s = tid; s < S; s += kPlanThreads) {
+  for (int s = tid; s < S; s += kPlanWorkers) {
     const int qs = __ldg(p.query_start_loc + s);
     const int q_len = __ldg(p.query_start_loc + s + 1) - qs;
     const int ctx = q_len < 1 ? 0 : seq_ctx(p, s, q_len);
@@ -297,9 +302,9 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     ctiles += __shfl_xor_sync(0xffffffffu, ctiles, o);
   }
   if (lane == 0) { s_red[warp][0] = pages; s_red[warp][1] = pairs; s_red[warp][2] = ctiles; }
-  __syncthreads();
+  sync();
   long long tp = 0, tq = 0, tt = 0;
-  for (int i = 0; i < kPlanThreads / 32; ++i) { tp += s_red[i][0]; tq += s_red[i][1]; tt += s_red[i][2]; }
+  for (int i = 0; i < kPlanWorkers / 32; ++i) { tp += s_red[i][0]; tq += s_red[i][1]; tt += s_red[i][2]; }
   const long long grid = w.grid;
   // decode pages per slice: about one slice per CTA, so most segments stay
   // whole (every slice pays a pipeline fill and a finalisation; a segment cut
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
 
   // pass 2: per-sequence counts, block exclusive scan over contiguous ranges;
   // slice counts per size bucket
-  const int per = ceil_div(S, kPlanThreads);
+  const int per = ceil_div(S, kPlanWorkers);
   const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
   int cd = 0, cc = 0;
   for (int s = s0; s < s1; ++s) {
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     if (lane >= o) { id += a; ic += b; }
   }
   if (lane == 31) { s_wd[warp] = id; s_wc[warp] = ic; }
-  __syncthreads();
+  sync();
   {
     int rd = 0, rc = 0;
     for (int i = 0; i < warp; ++i) { rd += s_wd[i]; rc += s_wc[i]; }
@@ -358,10 +363,10 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
       if (sq_len[s] == 1) rd += Hkv * pieces(s);
       else if (sq_len[s] > 1) rc += Hkv * units(s);
     }
-    if (tid == kPlanThreads - 1) { s_dec[S] = rd; s_chk[S] = rc; }
+    if (tid == kPlanWorkers - 1) { s_dec[S] = rd; s_chk[S] = rc; }
   }
   // bucket bases from the largest size down (one bucket per thread)
-  static_assert(kSizeBuckets == kPlanThreads, "one size bucket per plan thread");
+  static_assert(kSizeBuckets == kPlanWorkers, "one size bucket per plan thread");
   const int hb = kSizeBuckets - 1 - tid;  // thread 0 holds the largest bucket
   const int hc = s_hist[hb];
   int hi = hc;
@@ -370,19 +375,19 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     const int v = __shfl_up_sync(0xffffffffu, hi, o);
     if (lane >= o) hi += v;
   }
-  __syncthreads();  // s_wd of pass 2 read; s_dec, s_chk complete
+  sync();  // s_wd of pass 2 read; s_dec, s_chk complete
   if (lane == 31) s_wd[warp] = hi;
-  __syncthreads();
+  sync();
   {
     int base = 0;
     for (int i = 0; i < warp; ++i) base += s_wd[i];
     s_hist[hb] = base + hi - hc;
   }
-  __syncthreads();
+  sync();
   // each decode sequence takes the next places of its bucket
-  for (int s = tid; s < S; s += kPlanThreads)
+  for (int s = tid; s < S; s += kPlanWorkers)
     if (sq_len[s] == 1) s_pos[s] = atomicAdd(&s_hist[bucket(s)], Hkv * pieces(s));
-  __syncthreads();
+  sync();
   const int Nd = s_dec[S], Nc = s_chk[S];
   auto search = [&](const int *base, int k) {  // last s with base[s] <= k
     int lo = 0, hi2 = S - 1;
@@ -397,7 +402,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   // dynamic queue then fills the SMs the chunk units leave free with decode
   // slices from the start, and ends on the shortest slices.
   ItemDesc *list = reinterpret_cast<ItemDesc *>(w.list);
-  for (int k = tid; k < Nc; k += kPlanThreads) {
+  for (int k = tid; k < Nc; k += kPlanWorkers) {
     const int s = search(s_chk, k);
     const int q_len = sq_len[s];
     const int mt = ceil_div(q_len * G, BM), npair = (mt + 1) / 2;
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     d.c = k - u;
     list[k] = d;
   }
-  for (int i = tid; i < Nd; i += kPlanThreads) {
+  for (int i = tid; i < Nd; i += kPlanWorkers) {
     const int s = search(s_dec, i);
     const int n = ceil_div(sq_ctx[s], kPage), ks = pieces(s);
     const int local = i - s_dec[s];
@@ -433,8 +438,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     list[Nc + s_pos[s] + local] = d;
   }
   // merge counters of this step start at zero; so does the queue ticket
-  for (int x = tid; x < S * Hkv; x += kPlanThreads) w.dec_ctr[x] = 0u;
-  for (int x = tid; x < 2 * Nc; x += kPlanThreads) w.chunk_ctr[x] = 0u;
+  for (int x = tid; x < S * Hkv; x += kPlanWorkers) w.dec_ctr[x] = 0u;
+  for (int x = tid; x < 2 * Nc; x += kPlanWorkers) w.chunk_ctr[x] = 0u;
   if (tid == 0) {
     w.hdr[0] = Nc;
     w.hdr[1] = Nd;
@@ -690,9 +695,10 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     auto uwait = [&](uint64_t *bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity));
     };
+    // a CTA's first entry is its block index; later ones come from the ticket
     auto claim = [&]() -> int {
       int t = 0;
-      if (lane == 0) t = atomicAdd(w.hdr + 4, 1);
+      if (lane == 0) t = (int)gridDim.x + atomicAdd(w.hdr + 4, 1);
       return __shfl_sync(0xffffffffu, t, 0);
     };
     auto fetch = [&](int t, ItemDesc &d) -> bool {
@@ -714,9 +720,11 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     // The next item is claimed only once every copy of the current one has
     // been issued: the CTA is then close to free (which keeps the queue's
     // longest-first order dynamic), and the claim's latency hides behind the
-    // consumers' last queued tiles.
+    // consumers' last queued tiles.  The first entry needs no claim: CTA b
+    // takes entry b, so the step starts without a burst of atomics on the
+    // ticket and the longest entries go out in block order.
     ItemDesc dsc;
-    bool have = fetch(claim(), dsc);
+    bool have = fetch((int)blockIdx.x, dsc);
     for (;;) {
       WorkItem it;
       if (have) {
