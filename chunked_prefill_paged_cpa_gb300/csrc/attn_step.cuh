@@ -312,14 +312,17 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
   // tail short; at least 16 pages, a multiple of the 8-page block
   const int P = (int)max(16ll, ((tp + grid - 1) / grid + 7) / 8 * 8);
   // Chunk tile pairs are split over several units when they are fewer than
-  // the CTAs, so that no unit is longer than half of a CTA's share of the
-  // step's work: its chunk KV tiles and decode blocks (both 128-key blocks
-  // of attention) over the grid.  Without that, one long unit (a short chunk
-  // with a long cached prefix) would set the step's length on its own.
+  // the CTAs, so that no unit is longer than three quarters of a CTA's share
+  // of the step's work: its chunk KV tiles and decode blocks (both 128-key
+  // blocks of attention) over the grid.  Without that, one long unit (a short
+  // chunk with a long cached prefix) would set the step's length on its own;
+  // with smaller units, each one's partial result, merge and pipeline fill
+  // cost more than the balance they buy (measured: at half a share the
+  // default hybrid step took 117 us, at three quarters 105 us).
   // At most kMaxStepGrid units in all (the split-unit partials hold that many).
   const int nu = (tq == 0 || tq >= grid) ? 1 : (int)max(1ll, (long long)kMaxStepGrid / tq);
   const int unit_tiles =
-      (int)max((long long)kMinUnitTiles, ((tt + (tp + 7) / 8 + grid - 1) / grid + 1) / 2);
+      (int)max((long long)kMinUnitTiles, ((tt + (tp + 7) / 8 + grid - 1) / grid * 3 + 3) / 4);
   auto units = [&](int s) {  // chunk units of one kv head of sequence s
     const int mt = ceil_div(sq_len[s] * G, BM), npair = (mt + 1) / 2;
     return npair * min(nu, ceil_div(tile_kv<G>(sq_ctx[s], sq_len[s], mt - 1), unit_tiles));
