@@ -1029,9 +1029,55 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             if (ok && t > n_mine) ok = ack_v1(t - 1);
           }
         } else {
-          // decode: this pipeline reads blocks ti, ti + 2, ...; the other
-          // pipeline's blocks are observed and released in tile order as this
-          // one passes them
+          // decode: this pipeline reads blocks ti, ti + 2, ...  The item's
+          // fills are observed in the producer's order through a cursor: this
+          // pipeline's are released by the commit after the MMA that reads
+          // them, the other pipeline's with a plain arrival as soon as they are
+          // passed.  While it waits for its softmax's P, the issuer moves the
+          // cursor over every fill that has already landed, so the other
+          // pipeline's stages are released (and refilled) without waiting for
+          // this pipeline's next block.
+          const int nt = it.n_tiles;
+          int oc = 0;
+          auto fill_bars = [&](int f, uint64_t *&rdy, uint64_t *&emp, uint32_t &par) -> bool {
+            bool is_v;
+            int t;
+            fill_of(f, nt, is_v, t);
+            if (is_v) {
+              const int st = vr.stage(t);
+              rdy = &vready[st];
+              emp = &bs->v_empty[st];
+              par = vr.use(t) & 1;
+            } else {
+              const uint32_t kc = kvm + t;
+              rdy = &kready[kc % C::KST];
+              emp = &bs->k_empty[kc % C::KST];
+              par = (kc / C::KST) & 1;
+            }
+            return (t & 1) != ti;  // the other pipeline's fill
+          };
+          auto observe_through = [&](int last) -> bool {  // waits for each fill
+            for (; oc <= last && oc < 2 * nt; ++oc) {
+              uint64_t *rdy, *emp;
+              uint32_t par;
+              const bool other = fill_bars(oc, rdy, emp, par);
+              if (!ptx::mbar_wait(rdy, par)) return false;
+              if (other) ptx::mbar_arrive(emp);
+            }
+            return true;
+          };
+          auto observe_landed = [&]() {  // only the fills already ready
+            while (oc < 2 * nt) {
+              uint64_t *rdy, *emp;
+              uint32_t par;
+              const bool other = fill_bars(oc, rdy, emp, par);
+              if (!ptx::mbar_test(rdy, par)) break;
+              if (other) ptx::mbar_arrive(emp);
+              ++oc;
+            }
+          };
+          auto kfill = [&](int t) { return t == 0 ? 0 : 2 * t - 1; };                // fill index of K_t
+          auto vfill = [&](int t) { return t == nt - 1 ? 2 * nt - 1 : 2 * t + 2; };  // of V_t
           auto issue_qk = [&](uint32_t kvidx) {
             const uint32_t st = kvidx % C::KST;
 #pragma unroll
@@ -1046,8 +1092,7 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
           };
           if (ok && n_mine > 0) {
             const uint32_t kv0 = kvm + ti;
-            ok = (ti == 0 || ack_k1(0)) &&
-                 ptx::mbar_wait(&kready[kv0 % C::KST], (kv0 / C::KST) & 1) && lock();
+            ok = observe_through(kfill(ti)) && lock();
             if (ok) {
               ptx::tc_fence_after();
               issue_qk(kv0);
@@ -1061,13 +1106,17 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             const uint32_t kv = kvm + t;
             const int vst = vr.stage(t);
             const bool more = j + 1 < n_mine;
-            // the other pipeline's V of block t - 1 and K of block t + 1 come
-            // before this one's V of block t and K of block t + 2
-            if (!ptx::mbar_wait(&bs->p_full[ti], pcnt & 1) || (t > 0 && !ack_v1(t - 1)) ||
-                !ptx::mbar_wait(&vready[vst], vr.use(t) & 1) ||
-                (more && (!ack_k1(t + 1) ||
-                          !ptx::mbar_wait(&kready[(kv + 2) % C::KST], ((kv + 2) / C::KST) & 1))) ||
-                !lock()) {
+            // P_t, moving the cursor over landed fills meanwhile; then V_t and
+            // K_{t+2} with everything before them in the producer's order
+            bool got = false;
+            for (uint32_t i = 0; i < (1u << 22) && !got; ++i) {
+              got = ptx::mbar_test(&bs->p_full[ti], pcnt & 1);
+              if (!got) {
+                observe_landed();
+                got = ptx::mbar_try_wait(&bs->p_full[ti], pcnt & 1);
+              }
+            }
+            if (!got || !observe_through(more ? kfill(t + 2) : vfill(t)) || !lock()) {
               ok = false;
               break;
             }
@@ -1092,13 +1141,8 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
             }
             ptx::mma_commit(&bs->v_empty[vst]);
           }
-          // the other pipeline's blocks after this one's last (K_t before
-          // V_{t-1}, as the producer issues them)
-          const int done = n_mine > 0 ? ti + 2 * (n_mine - 1) + 1 : 0;  // tiles passed
-          for (int t = done; ok && t <= it.n_tiles; ++t) {
-            if (t < it.n_tiles && (t & 1) != ti) ok = ack_k1(t);
-            if (ok && t > done && ((t - 1) & 1) != ti) ok = ack_v1(t - 1);
-          }
+          // the rest of the item's fills (the other pipeline's last blocks)
+          if (ok) ok = observe_through(2 * nt - 1);
         }
         if (ok) {
           if (n_mine > 0) {
