@@ -727,7 +727,16 @@ attn_step_kernel(const AttnParams p, const StepWs w, const __grid_constant__ CUt
     // takes entry b, so the step starts without a burst of atomics on the
     // ticket and the longest entries go out in block order.
     ItemDesc dsc;
-    bool have = fetch((int)blockIdx.x, dsc);
+    bool have;
+    {
+      // entry b lies within the queue's capacity (at least kMaxStepGrid
+      // entries) whatever its size: load it alongside the size
+      const int4 *e = reinterpret_cast<const int4 *>(list + blockIdx.x);
+      const int4 x = __ldcg(e), y = __ldcg(e + 1);
+      have = (int)blockIdx.x < n_items;
+      dsc.s_kind = x.x; dsc.qs = x.y; dsc.ctx = x.z; dsc.q_len = x.w;
+      dsc.g_x = y.x; dsc.a = y.y; dsc.b = y.z; dsc.c = y.w;
+    }
     for (;;) {
       WorkItem it;
       if (have) {
