@@ -25,19 +25,22 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
 
 
-def _prepare(name, device):
+def _prepare(name, device, kv_e4m3=None):
     """A workload's first step with its new K/V already appended, and the
-    regular entry point's output on a zero-filled caller workspace."""
+    regular entry point's output on a zero-filled caller workspace
+    (``kv_e4m3`` = (k_scale, v_scale): an E4M3 cache)."""
     sc = workloads.scenario(name)
-    ws = workloads.WorkloadState(sc, device=device)
+    ws = workloads.WorkloadState(sc, device=device, kv_e4m3=kv_e4m3)
     inp = ws.step(0)
     m = inp["meta"]
     sh = sc.shape
-    ops.kv_append(inp["k"], inp["v"], m.slot_mapping, ws.k_cache, ws.v_cache)
-    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs, m.num_tokens)
+    kw = dict(k_scale=kv_e4m3[0], v_scale=kv_e4m3[1]) if kv_e4m3 else {}
+    ops.kv_append(inp["k"], inp["v"], m.slot_mapping, ws.k_cache, ws.v_cache, **kw)
+    wsp = ops.workspace_for(ws.k_cache, sh.num_q_heads, m.block_table.shape[1], m.num_seqs,
+                            m.num_tokens, inp["q"].dtype)
     assert wsp.numel() <= ops.cpa_noalloc_scratch_bytes()
     ref = ops.attention_forward(inp["q"], ws.k_cache, ws.v_cache, m.block_table,
-                                m.query_start_loc, m.seq_lens, sh.scale, wsp)
+                                m.query_start_loc, m.seq_lens, sh.scale, wsp, **kw)
     torch.cuda.synchronize()
     return sc, ws, inp, ref
 
@@ -45,7 +48,9 @@ def _prepare(name, device):
 def _noalloc(sc, ws, inp):
     m = inp["meta"]
     sh = sc.shape
-    desc = ops.make_desc(ws.k_cache, sh.num_q_heads, m.num_tokens, m.block_table.shape[1])
+    scales = ws.kv_e4m3 or (1.0, 1.0)
+    desc = ops.make_desc(ws.k_cache, sh.num_q_heads, m.num_tokens, m.block_table.shape[1],
+                         act_dtype=inp["q"].dtype, k_scale=scales[0], v_scale=scales[1])
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     out = torch.full_like(inp["q"], float("nan"))
     rc = ops.cpa_attention_forward_noalloc(
@@ -61,6 +66,16 @@ def _noalloc(sc, ws, inp):
 @pytest.mark.parametrize("name", ["tiny", "page1_default", "long_context", "decode_only"])
 def test_noalloc_equals_workspace_entry_point_twice(cuda_device, name):
     sc, ws, inp, ref = _prepare(name, cuda_device)
+    for _ in range(2):
+        out = _noalloc(sc, ws, inp)
+        assert torch.equal(_bits(out), _bits(ref))
+
+
+@pytest.mark.parametrize("name", ["page1_default", "decode_only"])
+def test_noalloc_e4m3_cache_equals_workspace_entry_point(cuda_device, name):
+    """With an E4M3 cache and bf16 queries the step also keeps the queries'
+    binary16 copy in its scratch."""
+    sc, ws, inp, ref = _prepare(name, cuda_device, workloads.E4M3_SCALES)
     for _ in range(2):
         out = _noalloc(sc, ws, inp)
         assert torch.equal(_bits(out), _bits(ref))
