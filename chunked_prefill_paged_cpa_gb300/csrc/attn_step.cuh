@@ -172,8 +172,8 @@ __device__ __forceinline__ int tile_kv(int ctx, int q_len, int m) {
   return (ctx - q_len + min(m * TM + TM - 1, q_len - 1)) / BN + 1;
 }
 
-// Queue entry written by the plan kernel (32 bytes).
-struct ItemDesc {
+// Queue entry written by the plan kernel (32 bytes, two 16-byte stores).
+struct __align__(16) ItemDesc {
   int s_kind;   // sequence | KIND_DECODE << 30
   int qs, ctx;
   int q_len;    // decode: pieces of the segment
@@ -435,8 +435,13 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(const AttnParam
     d.ctx = sq_ctx[s];
     d.q_len = ks;
     d.g_x = g | (piece << 8);
-    d.a = (int)((long long)piece * n / ks);
-    d.b = (int)((long long)(piece + 1) * n / ks);
+    if (n < 46341) {  // piece * n < 2^31: 32-bit division
+      d.a = piece * n / ks;
+      d.b = (piece + 1) * n / ks;
+    } else {
+      d.a = (int)((long long)piece * n / ks);
+      d.b = (int)((long long)(piece + 1) * n / ks);
+    }
     d.c = i;  // partial slot: the slice's own index, whatever its place
     list[Nc + s_pos[s] + local] = d;
   }
