@@ -289,11 +289,11 @@ def run_gpu(args, world, rank, local):
     # this library's kernels per step, as cpa_append_attention_forward
     # dispatches them: on the step path (bf16, head_dim 64/128, GQA group
     # 1/2/4/8) the plan kernel (which also does the append) and the persistent
-    # step kernel; otherwise the append and the row kernel
+    # step kernel; fp32: the append, the tf32 chunk kernel and the row kernel
     G = sh.num_q_heads // sh.num_kv_heads
     step_path = sh.dtype == torch.bfloat16 and sh.head_dim in (64, 128) and G in (1, 2, 4, 8)
     fused = step_path
-    launches_per_step = 2
+    launches_per_step = 2 if step_path else (3 if m.num_tokens >= 2 else 2)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     barrier(world)

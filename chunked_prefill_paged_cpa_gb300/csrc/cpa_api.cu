@@ -263,6 +263,11 @@ int attention(const void *q, const void *k_cache, const void *v_cache,
   p.part_o = reinterpret_cast<float *>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float2 *>(ws + w.part_ml);
   p.rows_mode = 0;
+  if (desc->dtype == CPA_F32) {
+    // the chunk rows on the tensor cores (tf32), the decode rows on the row kernel
+    if (launch_chunk_tf32(p, st) != cudaSuccess) return CPA_ERR_CUDA;
+    p.rows_mode = 2;
+  }
   return launch_attention_rows(p, desc->dtype, st) == cudaSuccess ? CPA_OK : CPA_ERR_CUDA;
 }
 

@@ -134,6 +134,10 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slots,
 
 cudaError_t launch_attention_rows(const AttnParams &p, int dtype, cudaStream_t stream);
 
+// fp32 steps: the chunk rows (q_len > 1) on the tensor cores, kind::tf32
+// (attn_chunk_tf32.cu); the decode rows then go to the row kernel (rows_mode 2).
+cudaError_t launch_chunk_tf32(const AttnParams &p, cudaStream_t stream);
+
 // Number of SMs of a device (cached); 0 if it cannot be queried.
 int sm_count(int device);
 

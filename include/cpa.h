@@ -154,7 +154,9 @@ int cpa_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
  * word.  Decodes with long contexts are split over the KV axis and merged in
  * the same launch with log-sum-exp weights ("Chunked Prefill 技术深度解析",
  * section 7.2: softmax normalised over the visible keys and combined
- * incrementally).  fp32 accumulation throughout; out has q's dtype. */
+ * incrementally).  fp32 accumulation throughout; out has q's dtype.  With
+ * fp32 activations the tensor cores round the chunk rows' MMA inputs to tf32
+ * (10 mantissa bits); decode rows are computed in fp32 on CUDA cores. */
 int cpa_attention_forward(const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_table,
                           const int32_t *query_start_loc, const int32_t *seq_lens,
