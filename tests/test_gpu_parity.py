@@ -171,6 +171,48 @@ def test_large_logit_jumps_rescale_and_redo(cuda_device):
     assert_close(out.cpu(), want, "planted logit jumps")
 
 
+def _jumps_inside_tiles(q, k_seqs, v_seqs):
+    """Sequence 0 (a chunk of 60 tokens after 340 cached): every query row is
+    one direction u per kv-head group, the other keys near-orthogonal; keys
+    40..47 are 1.0 u (a jump of ~16 log2 units in the second 32-key chunk of
+    the first 128-key tile), keys 200..203 are 3.0 u (~48, third chunk of the
+    second tile) and key 360 is 5.0 u (~80, fourth chunk of the third tile,
+    one of the chunk's own new rows): each moves the running maximum after
+    chunks of its tile were written."""
+    q, k0 = q.clone(), k_seqs[0].clone()
+    Hq, D = q.shape[1], q.shape[2]
+    Hkv = k0.shape[1]
+    G = Hq // Hkv
+    gen = torch.Generator().manual_seed(4343)
+    u = torch.randn(Hkv, D, generator=gen)
+    q[:60] = u.repeat_interleave(G, dim=0).to(q.dtype)[None]
+    k0 = (k0.float() * 0.05).to(k0.dtype)
+    k0[40:48] = u.to(k0.dtype)[None]
+    k0[200:204] = (3.0 * u).to(k0.dtype)[None]
+    k0[360] = (5.0 * u).to(k0.dtype)
+    return q, [k0] + list(k_seqs[1:]), v_seqs
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_logit_jumps_inside_a_tile_rescale_written_chunks(cuda_device, dtype):
+    q_lens, seq_lens = [60, 1], [400, 500]
+    Hq, Hkv, D = 8, 2, 128
+    st = make_step(q_lens, seq_lens, Hq, Hkv, D, dtype, seed=78,
+                   transform=_jumps_inside_tiles)
+    m, oc = st["meta"], st["oracle_cache"]
+    dev = cuda_device
+    k_cache, v_cache = oc.k.to(dev), oc.v.to(dev)
+    inp = {"meta": m.to(dev), "q": st["q"].to(dev), "k": st["k_new"].to(dev),
+           "v": st["v_new"].to(dev)}
+    scale = 1 / math.sqrt(D)
+    out, _ = gpu_step(k_cache, v_cache, inp, scale, Hq)
+    oracle_append(st)
+    want = oracle.attention(st["q"], oc.k, oc.v, m.block_table, m.query_start_loc,
+                            m.seq_lens, scale)
+    assert np.isfinite(out.float().cpu().numpy()).all()
+    assert_close(out.cpu(), want, f"jumps inside tiles ({dtype})")
+
+
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_every_chunk_kernel_shape(cuda_device, D, G):
