@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kTf32Threads, 1) attn_chunk_tf32_kernel(const 
   const int lr = mt * kTileRows + tid;
   const int tl = lr / G, t = qs + tl, h = g * G + (lr - tl * G);
   const int vis = ctx - q_len + tl + 1;  // keys the row sees
-  const bool valid = tl < q_len && vis > 0;
+  const bool valid = tl < q_len && t < p.num_tokens && vis > 0;  // (a token past the batch: malformed)
   const int vis_row = valid ? vis : 1;   // rows without output still see key 0 (finite math)
   // keys loaded: those the tile's last row sees (at least key 0)
   const int last_tl = (int)(min((int64_t)mt * kTileRows + kTileRows - 1, (int64_t)q_len * G - 1) / G);
